@@ -1,0 +1,7 @@
+"""fp64 CPU oracle of the LRM-pruned MoE expert backward (test infrastructure only).
+
+Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline / reference arm use it.
+"""
+from .lrm_oracle import (compact, expert_backward, expert_loads, lrm_scores, masked_backward,  # noqa: F401
+                         plan_quotas, pruned_backward, scatter_dx, select, swiglu_backward,
+                         unpruned_backward)

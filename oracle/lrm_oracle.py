@@ -1,0 +1,280 @@
+"""Oracle of the LRM-pruned MoE expert backward: plain, slow, obviously correct, fp64, CPU, numpy.
+
+TEST INFRASTRUCTURE. Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline /
+reference arm may import or run anything in this package. The product path (the
+CUDA library and its Python binding) never imports it and shares no code with it.
+
+Sources, all web pages about LRMoE (cited by title and section):
+  [EN] "LRMoE: Trimming Backward Work in Memory-Bound MoE Training" (aimodeling.com, English)
+  [ZH] the same article in Chinese (aimodeling.com), section "LRM:一个能分解的贡献度打分"
+  [PT] "LRMoE poda a passagem reversa do MoE e acelera o treinamento em 21–45%" (news.hamidun.com),
+       section "O que o LRMoE faz: forward completo, backward podado" (the five-step list)
+  [ES] "LRMoE recorta el paso hacia atrás de MoE y acelera el entrenamiento entre un 21 y un 45%",
+       section "Qué hace LRMoE: paso hacia delante completo, paso hacia atrás recortado"
+
+The method's result (a pruned gradient) is an approximation with no closed form of its
+own, so the oracle runs the algorithm's steps in the pages' order:
+  quotas -> LRM score -> per-expert top-quota selection -> physical compaction ->
+  grouped expert backward on the compacted rows -> back to the original token layout.
+Every library call below (np.lexsort, the @ matmul, np.exp) is a plain step of that
+definition; nothing is blocked, fused or reordered.
+
+Notation: T tokens, k routed experts per token, pair u = t*k + j (token-major), E experts,
+H hidden, I expert intermediate. h_u = [gate_u; up_u] (2I), phi_u = SiLU(gate_u)*up_u (I),
+W_gate_up[e] (2I x H, gate rows first), W_down[e] (H x I), upstream gradient g_t (H) of the
+layer output out_t = sum_j alpha_{t,j} W_down[e_{t,j}] phi_{t,j}.
+
+Readings where the pages are silent (each also listed in the design doc):
+  * phi is the input of the down projection, so G_u = (alpha_u g_t) phi_u^T is exactly
+    pair u's term of dW_down ("protected expert projection", [EN] "LRM: ...").
+  * A dropped pair contributes nothing to any part of the expert backward (dW_down,
+    dW_gate_up, dX): only retained rows are packed and computed ([EN] "The part that is
+    easy to get wrong"; [PT] step "Compactação física").
+  * Ties in score are broken by pair index u ascending; inside a segment the compacted
+    rows are in u ascending order.
+  * Quotas are integers; ratio rule quota = ceil(num/den * load) in exact integer math,
+    cap rule quota = min(load, cap); an explicit quota above the load keeps the whole load.
+
+Pins: every function here is checked in tests/test_oracle.py against something other
+than itself (see each docstring). Nothing here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import numpy as np
+
+
+# ----------------------------------------------------------------------------------------
+# quotas  ([EN] "Backward demand is not a constant": before the expert forward the
+# controller looks at each expert's routed demand and fixes a retention quota that holds
+# for the whole layer call; [PT] second bullet)
+# ----------------------------------------------------------------------------------------
+def expert_loads(topk_idx, E):
+    """load_e = number of routed pairs whose expert is e.
+    Pinned: the articles' example loads [4, 2, 3] (tests/golden/load_example.json)."""
+    flat = np.asarray(topk_idx).reshape(-1).astype(np.int64)
+    return np.bincount(flat, minlength=E).astype(np.int64)
+
+
+def plan_quotas(topk_idx, E, kind, num=0, den=1, cap=0, explicit=None):
+    """Per-expert retention quota.
+    ratio: ceil(num/den * load) computed as (num*load + den - 1) // den;
+    cap:   min(load, cap);
+    explicit: the given list, unchanged (selection keeps min(quota, load)).
+    Pinned: exact-rational ceil/min over every load up to 10^6 and the worked example."""
+    loads = expert_loads(topk_idx, E)
+    if kind == "ratio":
+        quotas = (num * loads + den - 1) // den
+    elif kind == "cap":
+        quotas = np.minimum(loads, cap)
+    elif kind == "explicit":
+        quotas = np.asarray(explicit, dtype=np.int64).copy()
+        assert quotas.shape == (E,)
+    else:
+        raise ValueError(kind)
+    return loads, quotas.astype(np.int64)
+
+
+# ----------------------------------------------------------------------------------------
+# LRM score  ([EN] "LRM: a decomposable contribution score": G_u = (alpha_u g_t) phi_u^T is
+# rank one, so ||G_u||_F^2 splits into routing strength alpha_u^2, backward signal
+# ||g_t||^2 and expert-state magnitude ||phi_u||^2; [PT] "Seleção pela métrica LRM")
+# ----------------------------------------------------------------------------------------
+def lrm_scores(alpha, g, phi):
+    """R[t, j] = alpha[t,j]^2 * ||g_t||_2^2 * ||phi[t,j]||_2^2 in fp64.
+    alpha [T,k], g [T,H], phi [T,k,I] -> R [T,k].
+    Pinned: equals the squared Frobenius norm of the explicit H x I outer product."""
+    a = np.asarray(alpha, dtype=np.float64)
+    gg = np.asarray(g, dtype=np.float64)
+    pp = np.asarray(phi, dtype=np.float64)
+    g_sq = np.sum(gg * gg, axis=1)            # ||g_t||^2, [T]
+    phi_sq = np.sum(pp * pp, axis=2)          # ||phi_u||^2, [T,k]
+    return (a * a) * g_sq[:, None] * phi_sq
+
+
+# ----------------------------------------------------------------------------------------
+# selection  ([PT]/[ES] "Seleção pela métrica LRM": inside the quota the highest-scoring
+# pairs are kept; [EN] "Three things worth flagging": the guarantee covers an additive
+# local objective, i.e. the kept set maximises the kept score sum per expert)
+# ----------------------------------------------------------------------------------------
+def select(topk_idx, scores, quotas, E):
+    """Keep, per expert e, the min(quota_e, load_e) pairs with the largest score, ties to
+    the smaller u.  Returns
+      seg_offsets int64 [E+1]: exclusive prefix sum of the kept counts,
+      kept_pair   int64 [R]:   kept pairs, expert-major, u ascending inside a segment,
+      row_of_pair int64 [P]:   compacted row of each pair, -1 if dropped.
+    Works on any score dtype (fp64 oracle scores, or fp32 scores compared exactly).
+    Pinned: brute force over all subsets on small segments; the worked example."""
+    flat_idx = np.asarray(topk_idx).reshape(-1).astype(np.int64)
+    s = np.asarray(scores).reshape(-1)
+    P = flat_idx.shape[0]
+    q = np.asarray(quotas, dtype=np.int64)
+    seg_offsets = np.zeros(E + 1, dtype=np.int64)
+    kept_lists = []
+    for e in range(E):
+        pairs = np.nonzero(flat_idx == e)[0]            # u ascending
+        keep_n = int(min(max(q[e], 0), pairs.shape[0]))
+        # order by score descending, then u ascending (lexsort: last key is primary)
+        order = np.lexsort((pairs, -s[pairs]))
+        kept = np.sort(pairs[order[:keep_n]])
+        kept_lists.append(kept)
+        seg_offsets[e + 1] = seg_offsets[e] + keep_n
+    kept_pair = np.concatenate(kept_lists) if kept_lists else np.zeros(0, np.int64)
+    row_of_pair = np.full(P, -1, dtype=np.int64)
+    row_of_pair[kept_pair] = np.arange(kept_pair.shape[0], dtype=np.int64)
+    return seg_offsets, kept_pair.astype(np.int64), row_of_pair
+
+
+# ----------------------------------------------------------------------------------------
+# physical compaction  ([EN] "The part that is easy to get wrong": retained gradient rows
+# and their saved activations are repacked into contiguous expert-specific buffers, with
+# no padding; [PT] "Compactação física")
+# ----------------------------------------------------------------------------------------
+def compact(kept_pair, alpha, g, x, h, phi, k):
+    """Gather the kept pairs' rows, in kept_pair order, in fp64:
+      dY_c[r] = alpha_u * g_t,  X_c[r] = x_t,  H_c[r] = h_u,  Phi_c[r] = phi_u  (u = kept_pair[r], t = u // k).
+    Pinned: the compacted backward equals the full-shape backward with dropped pairs'
+    gradient rows zero-masked (the articles' negative result: masking gives the same
+    numbers, only without the saving)."""
+    kp = np.asarray(kept_pair, dtype=np.int64)
+    t = kp // k
+    a = np.asarray(alpha, dtype=np.float64).reshape(-1)[kp]
+    gg = np.asarray(g, dtype=np.float64)[t]
+    dY_c = a[:, None] * gg
+    X_c = np.asarray(x, dtype=np.float64)[t]
+    hh = np.asarray(h, dtype=np.float64)
+    H_c = hh.reshape(-1, hh.shape[-1])[kp]
+    pp = np.asarray(phi, dtype=np.float64)
+    Phi_c = pp.reshape(-1, pp.shape[-1])[kp]
+    return dY_c, X_c, H_c, Phi_c
+
+
+# ----------------------------------------------------------------------------------------
+# grouped expert backward on the compacted rows  ([EN] "The part that is easy to get
+# wrong": the retained row counts drive variable-size grouped GEMMs; the expert is the
+# SwiGLU MLP whose down projection consumes phi)
+# ----------------------------------------------------------------------------------------
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def swiglu_backward(dphi, gate, up):
+    """phi = SiLU(gate) * up, SiLU(z) = z * sigmoid(z).  With s = sigmoid(gate):
+      d phi / d up   = gate * s
+      d phi / d gate = up * (s + gate * s * (1 - s)) = up * s * (1 + gate * (1 - s)).
+    Pinned: central finite differences in fp64, and torch fp64 autograd."""
+    s = sigmoid(gate)
+    dgate = dphi * up * s * (1.0 + gate * (1.0 - s))
+    dup = dphi * gate * s
+    return dgate, dup
+
+
+def expert_backward(seg_offsets, dY_c, X_c, H_c, Phi_c, w_gate_up, w_down):
+    """For each expert e over its segment rows (R_e of them):
+      dW_down[e]    = dY_c[e]^T Phi_c[e]                         (H x I)
+      dPhi          = dY_c[e] W_down[e]                          (R_e x I)
+      [dgate; dup]  = SwiGLU backward of dPhi at H_c[e]          (R_e x 2I)
+      dW_gate_up[e] = [dgate; dup]^T X_c[e]                      (2I x H)
+      dX_c[e]       = [dgate; dup] W_gate_up[e]                  (R_e x H)
+    An expert with no rows gets dW = 0.
+    Pinned: with quota = load it equals torch fp64 autograd of the explicit forward."""
+    E = len(seg_offsets) - 1
+    Wgu = np.asarray(w_gate_up, dtype=np.float64)
+    Wd = np.asarray(w_down, dtype=np.float64)
+    H = Wd.shape[1]
+    I = Wd.shape[2]
+    R = dY_c.shape[0]
+    dW_down = np.zeros((E, H, I))
+    dW_gate_up = np.zeros((E, 2 * I, H))
+    dH_c = np.zeros((R, 2 * I))
+    dX_c = np.zeros((R, H))
+    for e in range(E):
+        r0, r1 = int(seg_offsets[e]), int(seg_offsets[e + 1])
+        if r1 == r0:
+            continue
+        dy = dY_c[r0:r1]
+        dW_down[e] = dy.T @ Phi_c[r0:r1]
+        dphi = dy @ Wd[e]
+        dgate, dup = swiglu_backward(dphi, H_c[r0:r1, :I], H_c[r0:r1, I:])
+        dh = np.concatenate([dgate, dup], axis=1)
+        dH_c[r0:r1] = dh
+        dW_gate_up[e] = dh.T @ X_c[r0:r1]
+        dX_c[r0:r1] = dh @ Wgu[e]
+    return dW_gate_up, dW_down, dH_c, dX_c
+
+
+# ----------------------------------------------------------------------------------------
+# back to the original layout  ([PT] "Depois, o resultado volta ao layout original")
+# ----------------------------------------------------------------------------------------
+def scatter_dx(row_of_pair, dX_c, T, k):
+    """dX[t] = sum over j = 0..k-1 (in that order) of dX_c[row_of_pair[t*k+j]] for kept pairs;
+    a token with no kept pair gets 0.
+    Pinned: with quota = load the whole path equals torch fp64 autograd's dL/dx."""
+    rop = np.asarray(row_of_pair, dtype=np.int64).reshape(T, k)
+    H = dX_c.shape[1]
+    dX = np.zeros((T, H))
+    for j in range(k):
+        rows = rop[:, j]
+        m = rows >= 0
+        dX[m] += dX_c[rows[m]]
+    return dX
+
+
+# ----------------------------------------------------------------------------------------
+# the whole path
+# ----------------------------------------------------------------------------------------
+def pruned_backward(inp, quotas, scores=None):
+    """Run score -> select -> compact -> grouped backward -> scatter on the inputs dict
+    (numpy or torch CPU arrays: topk_idx [T,k], alpha [T,k], x [T,H], g [T,H], h [T,k,2I],
+    phi [T,k,I], w_gate_up [E,2I,H], w_down [E,H,I]).  `scores` overrides the fp64 scores
+    used for selection (e.g. the GPU's fp32 scores, for the bit-exact selection check)."""
+    idx = _np(inp["topk_idx"])
+    T, k = idx.shape
+    E = _np(inp["w_down"]).shape[0]
+    R_u = lrm_scores(_np(inp["alpha"]), _np(inp["g"]), _np(inp["phi"]))
+    sel_scores = R_u if scores is None else _np(scores)
+    seg, kept, rop = select(idx, sel_scores, quotas, E)
+    dY_c, X_c, H_c, Phi_c = compact(kept, _np(inp["alpha"]), _np(inp["g"]), _np(inp["x"]),
+                                    _np(inp["h"]), _np(inp["phi"]), k)
+    dWgu, dWd, dH_c, dX_c = expert_backward(seg, dY_c, X_c, H_c, Phi_c,
+                                            _np(inp["w_gate_up"]), _np(inp["w_down"]))
+    dX = scatter_dx(rop, dX_c, T, k)
+    return {"scores": R_u, "seg_offsets": seg, "kept_pair": kept, "row_of_pair": rop,
+            "dY_c": dY_c, "X_c": X_c, "H_c": H_c, "Phi_c": Phi_c,
+            "dH_c": dH_c, "dX_c": dX_c, "dw_gate_up": dWgu, "dw_down": dWd, "dx": dX}
+
+
+def unpruned_backward(inp):
+    """The ordinary expert backward over every routed pair (quota = load)."""
+    idx = _np(inp["topk_idx"])
+    E = _np(inp["w_down"]).shape[0]
+    loads = expert_loads(idx, E)
+    return pruned_backward(inp, loads)
+
+
+def masked_backward(inp, quotas):
+    """Full-shape backward: every routed pair is processed, dropped pairs' gradient rows
+    are zero-masked instead of removed (the articles' 'selection without compaction')."""
+    idx = _np(inp["topk_idx"])
+    T, k = idx.shape
+    E = _np(inp["w_down"]).shape[0]
+    R_u = lrm_scores(_np(inp["alpha"]), _np(inp["g"]), _np(inp["phi"]))
+    _, _, rop = select(idx, R_u, quotas, E)
+    loads = expert_loads(idx, E)
+    seg_all, all_pairs, rop_all = select(idx, R_u, loads, E)
+    dY, X, Hh, Phi = compact(all_pairs, _np(inp["alpha"]), _np(inp["g"]), _np(inp["x"]),
+                             _np(inp["h"]), _np(inp["phi"]), k)
+    dropped = rop[all_pairs] < 0
+    dY[dropped] = 0.0
+    dWgu, dWd, dH, dX_rows = expert_backward(seg_all, dY, X, Hh, Phi,
+                                             _np(inp["w_gate_up"]), _np(inp["w_down"]))
+    dX = scatter_dx(rop_all, dX_rows, T, k)
+    return {"dw_gate_up": dWgu, "dw_down": dWd, "dx": dX}
+
+
+def _np(a):
+    if hasattr(a, "detach"):
+        a = a.detach().cpu()
+        if a.dtype.is_floating_point:
+            a = a.double()
+        return a.numpy()
+    return np.asarray(a)
