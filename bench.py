@@ -1,0 +1,444 @@
+#!/usr/bin/env python3
+"""Throughput of the LRM-pruned MoE expert backward on GB300: retained pairs/s.
+
+One step = one pass of the whole hot path (score -> select -> compact -> grouped SwiGLU
+expert backward -> scatter dX) over one batch of seeded synthetic input that is already
+resident in HBM.  Default workload: the Qwen3-30B-A3B-shaped layer, T=8192, H=2048,
+I=768, E=128, top-8, bf16, drop 20 % (quota = ceil(0.8 * load)).
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+       [--workload NAME] [--no-cpu-baseline]
+Under torchrun (N > 1) every rank runs an independent batch (weak scaling, no collective on
+the data path; a barrier brackets the timed region and the slowest rank's time is used).
+
+--impl reference times the fp64 CPU oracle (the plain restatement of the method) on the
+host cores, each step a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "retained pairs/s through pruned expert backward; % of BF16 TC / HBM roofline"
+UNIT = "pairs/s"
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]), "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def quota_text(wl):
+    q = wl.quota
+    if q[0] == "ratio":
+        return f"ceil({q[1]}/{q[2]} * load_e)"
+    if q[0] == "cap":
+        return f"min(load_e, {q[1]})"
+    return f"explicit {list(q[1])}"
+
+
+# ------------------------------------------------------------------ byte / flop models ----
+def algorithmic(wl, R, T_any):
+    """Bytes (or flops) each stage must move (or do).  b = element bytes; R retained rows;
+    T_any tokens with at least one kept pair (compaction reads g_t, x_t once per such token)."""
+    T, H, I, E, k = wl.T, wl.H, wl.I, wl.E, wl.k
+    P = T * k
+    b = 2 if wl.dtype == "bf16" else 4
+    return {
+        "score": {"bytes": T * H * b + P * I * b + 4 * P + 4 * P},
+        "select": {"bytes": 4 * P * 2 + 4 * P * 2 + 4 * P + 4 * R + 4 * (E + 1)},
+        "compact": {"bytes": T_any * 2 * H * b + R * 3 * I * b + R * (2 * H + 3 * I) * b + 4 * P + 4 * P},
+        "grouped": {"flops": 12 * H * I * R,
+                    "bytes": R * (H + I) * b + 4 * E * H * I            # dW_down
+                    + R * H * b + E * H * I * b + 2 * R * 2 * I * b     # dphi + SwiGLU
+                    + R * (2 * I + H) * b + 8 * E * I * H               # dW_gate_up
+                    + R * 2 * I * b + 2 * E * I * H * b + R * H * b},   # dX_c
+        "scatter": {"bytes": R * H * b + T * H * b + 4 * P},
+    }
+
+
+# ------------------------------------------------------------------ clocks ----------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.proc = None
+        self.path = os.path.join("/tmp", f"lrm_clocks_{os.getpid()}.csv")
+        try:
+            uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+            self.sel = ["-i", uuid if uuid.startswith("GPU-") else "GPU-" + uuid]
+        except Exception:
+            self.sel = []
+
+    def start(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", *self.sel, f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ traffic record --------
+def recorded_traffic(kernel_stage):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
+    source of that kernel (the summary stores a hash of the kernel's source file)."""
+    path = os.path.join(ROOT, "profiles", "traffic.txt")
+    if not os.path.exists(path):
+        return None
+    for line in open(path):
+        m = re.match(r"\s*stage=(\S+)\s+workload=(\S+)\s+source=(\S+)\s+sha=(\S+)\s+dram_bytes=(\d+)", line)
+        if not m or m.group(1) != kernel_stage:
+            continue
+        src = os.path.join(ROOT, m.group(3))
+        if not os.path.exists(src):
+            return None
+        if hashlib.sha256(open(src, "rb").read()).hexdigest()[:16] != m.group(4):
+            return None
+        return {"workload": m.group(2), "bytes": int(m.group(5))}
+    return None
+
+
+# ------------------------------------------------------------------ oracle timing ---------
+def oracle_sample(wl, cpu_inp, quotas_np, target_s=15.0):
+    """Time the fp64 oracle on a leading slice of the tokens; returns (pairs/s, info)."""
+    import oracle
+    T = wl.T
+    ts = min(T, 512)
+    while True:
+        sub = {n: (v[:ts] if n not in ("w_gate_up", "w_down") else v) for n, v in cpu_inp.items()}
+        loads, q = oracle.plan_quotas(sub["topk_idx"].numpy(), wl.E, *W.quota_policy(wl)[:4],
+                                      explicit=W.quota_policy(wl)[4])
+        t0 = time.perf_counter()
+        out = oracle.pruned_backward(sub, q)
+        dt = time.perf_counter() - t0
+        R = int(out["seg_offsets"][-1])
+        if dt >= target_s / 4 or ts >= T:
+            return R / dt, {"tokens": ts, "retained": R, "seconds": dt}
+        ts = min(T, int(ts * max(2.0, min(8.0, target_s / 2 / max(dt, 1e-3)))))
+
+
+def cpu_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
+        if n:
+            return n
+    except Exception:
+        pass
+    return os.cpu_count()
+
+
+# ------------------------------------------------------------------ main -------------------
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="qwen3_t8k_d20", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05 (comparison only)")
+    args = ap.parse_args()
+    assert args.warmup >= 3, "at least 3 warm-up steps"
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    wl = W.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        return reference_arm(args, wl, rank, world)
+
+    import pruned_expert_backward_gb300 as lrm
+    from pruned_expert_backward_gb300 import _lib
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+        pg = dist
+
+    inp = W.generate(wl, dev, seed=rank)
+    kind, num, den, cap, expl = W.quota_policy(wl)
+    ex = None if expl is None else torch.tensor(expl, dtype=torch.int32, device=dev)
+    loads, quotas = lrm.lrm_plan_quotas(inp["topk_idx"], wl.E, kind, num, den, cap, explicit=ex)
+    flags = _lib.LRM_GEMM_FORCE_SIMT if (args.simt or wl.dtype == "f32") else _lib.LRM_GEMM_DEFAULT
+    pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, device=dev, flags=flags)
+    stream = torch.cuda.current_stream()
+
+    stages = ["score", "select", "compact", "grouped", "scatter"]
+
+    def step(evs=None):
+        if evs is not None:
+            evs[0].record(stream)
+        lrm.lrm_score(inp["alpha"], inp["g"], inp["phi"], scores=pb.scores, dev_status=pb.dev_status)
+        if evs is not None:
+            evs[1].record(stream)
+        lrm.lrm_select(inp["topk_idx"], pb.scores, quotas, wl.E, cap=pb.cap, seg_offsets=pb.seg_offsets,
+                       kept_pair=pb.kept_pair, row_of_pair=pb.row_of_pair, ws=pb.ws, dev_status=pb.dev_status)
+        if evs is not None:
+            evs[2].record(stream)
+        lrm.lrm_compact(pb.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], pb.cap,
+                        dy_c=pb.dy_c, x_c=pb.x_c, h_c=pb.h_c, phi_c=pb.phi_c)
+        if evs is not None:
+            evs[3].record(stream)
+        lrm.lrm_grouped_backward(pb.seg_offsets, pb.dy_c, pb.x_c, pb.h_c, pb.phi_c, inp["w_gate_up"],
+                                 inp["w_down"], pb.cap, dw_gate_up=pb.dw_gate_up, dw_down=pb.dw_down,
+                                 dh_c=pb.dh_c, dx_c=pb.dx_c, ws=pb.ws, flags=flags, dev_status=pb.dev_status)
+        if evs is not None:
+            evs[4].record(stream)
+        lrm.lrm_scatter_dx(pb.row_of_pair, pb.dx_c, wl.T, wl.k, dx=pb.dx)
+        if evs is not None:
+            evs[5].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    st = int(pb.dev_status.item())
+    if st != 0:
+        raise SystemExit(f"device status {st} after warm-up")
+    R = int(pb.seg_offsets[-1].item())
+    rop = pb.row_of_pair.view(wl.T, wl.k)
+    T_any = int((rop >= 0).any(dim=1).sum().item())
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(args.steps)]
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record(stream)
+    for i in range(args.steps):
+        step(evs[i])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    clk = clocks.stop()
+    total_ms = t_start.elapsed_time(t_end)
+    if pg:
+        t = torch.tensor([total_ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        total_ms = float(t.item())
+        r_all = torch.tensor([R], device=dev, dtype=torch.float64)
+        pg.all_reduce(r_all)
+        R_total = float(r_all.item())
+    else:
+        R_total = float(R)
+    stage_ms = {s: 0.0 for s in stages}
+    for e in evs:
+        for j, s in enumerate(stages):
+            stage_ms[s] += e[j].elapsed_time(e[j + 1])
+    stage_ms = {s: v / args.steps for s, v in stage_ms.items()}
+    ms_per_step = total_ms / args.steps
+    value = R_total * args.steps / (total_ms / 1e3)
+
+    # ---- end-to-end through the public API with pinned host buffers ------------------------
+    e2e = end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev)
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return
+
+    pk = peaks()
+    alg = algorithmic(wl, R, T_any)
+    stage_info = {}
+    for s in stages:
+        ms = stage_ms[s]
+        d = {"ms": round(ms, 4)}
+        if "bytes" in alg[s]:
+            gbs = alg[s]["bytes"] / (ms / 1e3) / 1e9
+            d.update({"alg_bytes": alg[s]["bytes"], "GB/s": round(gbs, 1),
+                      "frac_hbm": round(gbs / pk["hbm_gbs"], 4)})
+        if "flops" in alg[s]:
+            tf = alg[s]["flops"] / (ms / 1e3) / 1e12
+            d.update({"alg_flops": alg[s]["flops"], "TFLOP/s": round(tf, 1),
+                      "frac_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4)})
+        stage_info[s] = d
+    dom = max(stages, key=lambda s: stage_ms[s])
+    tr = recorded_traffic(dom)
+    if "flops" in alg[dom] and wl.dtype == "bf16":
+        ach = alg[dom]["flops"] / (stage_ms[dom] / 1e3) / 1e12
+        roof = {"bound": "tensor", "kernel": f"lrm_grouped_backward ({dom})", "achieved": round(ach, 2),
+                "peak": pk["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(ach / pk["bf16_tflops_sustained"], 4),
+                "peak_kind": f"bf16 dense, sustained, {pk['source']}"}
+    else:
+        ach = alg[dom]["bytes"] / (stage_ms[dom] / 1e3) / 1e9
+        roof = {"bound": "hbm", "kernel": dom, "achieved": round(ach, 1), "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": round(ach / pk["hbm_gbs"], 4), "peak_kind": f"HBM copy, {pk['source']}"}
+    roof["traffic"] = tr["bytes"] if tr else None
+    if tr:
+        roof["traffic_workload"] = tr["workload"]
+
+    launches = pb_launches(wl, flags)
+    out = {
+        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": wl.dtype, "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "pairs": wl.P, "retained_pairs": R, "quota": quota_text(wl), "zipf_s": wl.zipf_s,
+                   "gemm": "simt" if flags else "tcgen05", "parallelism": f"replicas{world}" if world > 1 else "1gpu",
+                   "l2": "no flush: every step streams > 1 GB (inputs, compacted buffers, weights, fp32 dW) "
+                         "through a 129 MB L2"},
+        "roofline": roof,
+        "stages": stage_info,
+        "e2e": e2e,
+        "gpu_launches": launches * args.steps,
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        cpu_inp = {n: v.cpu() for n, v in inp.items()}
+        v, info = oracle_sample(wl, cpu_inp, None)
+        out["cpu_baseline"] = {"value": round(v, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                               "sample": f"fp64 numpy oracle, whole path on the first {info['tokens']} of "
+                                         f"{wl.T} tokens ({info['retained']} retained pairs, "
+                                         f"{info['seconds']:.1f} s)"}
+    print(json.dumps(out), flush=True)
+    if pg:
+        pg.destroy_process_group()
+
+
+def pb_launches(wl, flags):
+    """Kernels this library launches per step (memsets excluded)."""
+    sel = 4 if wl.P > 0 else 1
+    grouped = 4 if flags else 2
+    return 1 + sel + 1 + grouped + 1
+
+
+def end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev):
+    """Same metric through the public API, with the step's inputs copied in from pinned host
+    memory and its result (dX and the segment offsets) read back, every step."""
+    names = ["topk_idx", "alpha", "x", "g", "h", "phi"]
+    host = {n: inp[n].cpu().pin_memory() for n in names}
+    host_q = quotas.cpu().pin_memory()
+    out_dx = torch.empty_like(pb.dx, device="cpu").pin_memory()
+    out_seg = torch.empty_like(pb.seg_offsets, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values()) + host_q.numel() * 4
+    d2h = out_dx.numel() * out_dx.element_size() + out_seg.numel() * 4
+    steps = max(3, min(args.steps, 20))
+
+    def one():
+        for n in names:
+            inp[n].copy_(host[n], non_blocking=True)
+        quotas.copy_(host_q, non_blocking=True)
+        step()
+        out_dx.copy_(pb.dx, non_blocking=True)
+        out_seg.copy_(pb.seg_offsets, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        return int(out_seg[-1])
+
+    for _ in range(3):
+        one()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b)
+    if pg:
+        t = torch.tensor([ms], device=dev)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    return {"value": round(R_total * steps / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4)}
+
+
+def reference_arm(args, wl, rank, world):
+    """fp64 CPU oracle on the host cores: each step is a bounded sample of the workload."""
+    if rank != 0:
+        return
+    import oracle
+    # inputs drawn on the CPU with the same generator (the oracle never touches the GPU)
+    ts = min(wl.T, 1024 if wl.H * wl.I <= 2048 * 768 else 512)
+    sub_wl = wl if ts == wl.T else W.Workload(wl.name + "_sample", ts, wl.H, wl.I, wl.E, wl.k, wl.dtype,
+                                              wl.zipf_s, wl.g_std, wl.quota)
+    inp = W.generate(sub_wl, "cpu", seed=0)
+    kind, num, den, cap, expl = W.quota_policy(wl)
+    _, q = oracle.plan_quotas(inp["topk_idx"].numpy(), wl.E, kind, num, den, cap, expl)
+    for _ in range(args.warmup):
+        oracle.pruned_backward(inp, q)
+    t0 = time.perf_counter()
+    R = 0
+    for _ in range(args.steps):
+        R = int(oracle.pruned_backward(inp, q)["seg_offsets"][-1])
+    dt = time.perf_counter() - t0
+    value = R * args.steps / dt
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
+                   "quota": quota_text(wl), "sample_tokens": ts},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+                         "sample": f"fp64 numpy oracle, whole path on {ts} of {wl.T} tokens per step "
+                                   f"({R} retained pairs)"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+if __name__ == "__main__":
+    main()

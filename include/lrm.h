@@ -1,0 +1,185 @@
+/*
+ * lrm.h — C ABI of the LRM-pruned MoE expert backward on one GPU (sm_103a).
+ *
+ * The operation is the expert-layer backward of LRMoE, as described in
+ *   "LRMoE: Trimming Backward Work in Memory-Bound MoE Training" (aimodeling.com), sections
+ *   "Backward demand is not a constant", "LRM: a decomposable contribution score" and
+ *   "The part that is easy to get wrong", and in the five-step list of
+ *   "LRMoE poda a passagem reversa do MoE e acelera o treinamento em 21–45%" (news.hamidun.com),
+ *   section "O que o LRMoE faz: forward completo, backward podado":
+ *     quotas -> LRM score -> keep each expert's top-quota pairs -> physical compaction ->
+ *     variable-size grouped GEMMs -> result back to the original layout.
+ *
+ * Notation.  T tokens, k routed experts per token, P = T*k pairs, pair u = t*k + j
+ * (token-major), E experts, H hidden, I expert intermediate, R_e retained rows of expert e,
+ * R = sum_e R_e.  The expert is a SwiGLU MLP: h_u = W_gate_up[e] x_t = [gate_u; up_u] (2I),
+ * phi_u = SiLU(gate_u) * up_u (I), output alpha_u W_down[e] phi_u; g_t (H) is the upstream
+ * gradient of the layer output.
+ *
+ * Conventions shared by every entry point.
+ *  - Every call is asynchronous on the caller's stream (NULL = legacy default stream). The
+ *    library never allocates, frees or synchronises; a call returns after its launches are
+ *    queued.
+ *  - Every pointer argument is caller-owned DEVICE memory unless stated otherwise, aligned
+ *    to 16 bytes, and must stay valid until the stream work completes.  The library keeps
+ *    no pointer after a call returns.
+ *  - Row-major, densely packed tensors.  lrm_dtype fixes the element type of g, x, h, phi,
+ *    the weights, the compacted buffers and dX; alpha and scores are always fp32, indices
+ *    are int32, weight gradients are always fp32.
+ *  - Host-detected errors are returned (nothing is launched, outputs are untouched).
+ *    Device-detected errors are written to the optional `dev_status` word (int32, device
+ *    memory, caller zeroes it): the first error code wins (atomic compare-and-swap from 0).
+ *    The caller reads it whenever it chooses; the library never does.
+ *  - Limits: 1 <= E <= LRM_MAX_EXPERTS, 1 <= k <= LRM_MAX_TOPK, P <= INT32_MAX,
+ *    H and I positive multiples of 8.
+ */
+#ifndef LRM_H
+#define LRM_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define LRM_MAX_EXPERTS 1024
+#define LRM_MAX_TOPK 16
+
+typedef enum lrm_status {
+  LRM_OK = 0,
+  LRM_ERR_INVALID_ARG = 1, /* null pointer, misaligned pointer, negative size, bad enum   */
+  LRM_ERR_SHAPE = 2,       /* a size outside the limits above                           */
+  LRM_ERR_DTYPE = 3,       /* unknown lrm_dtype                                         */
+  LRM_ERR_WORKSPACE = 4,   /* workspace null or smaller than lrm_workspace_size         */
+  LRM_ERR_CUDA = 5,        /* a CUDA launch/runtime call failed                         */
+  LRM_ERR_CAPACITY = 6,    /* device: sum of kept rows exceeds `cap` (nothing is kept)  */
+  LRM_ERR_NONFINITE = 7,   /* device: a score is NaN or infinite                        */
+  LRM_ERR_TIMEOUT = 8,     /* device: a bounded wait gave up                            */
+  LRM_ERR_BAD_INDEX = 9,   /* device: an expert id outside [0, E) (pair treated as dropped) */
+  LRM_ERR_UNSUPPORTED = 10 /* no kernel for this device / configuration                 */
+} lrm_status;
+
+typedef enum lrm_dtype { LRM_BF16 = 0, LRM_F32 = 1 } lrm_dtype;
+
+typedef enum lrm_quota_kind {
+  LRM_QUOTA_RATIO = 0,    /* quota_e = ceil(num/den * load_e), exact integer arithmetic   */
+  LRM_QUOTA_CAP = 1,      /* quota_e = min(load_e, cap)                                   */
+  LRM_QUOTA_EXPLICIT = 2  /* quota_e = explicit_quotas[e] (copied)                        */
+} lrm_quota_kind;
+
+/* Flags of lrm_grouped_backward. */
+#define LRM_GEMM_DEFAULT 0     /* tcgen05 tensor-core kernels for bf16, SIMT fp32 kernels for fp32 */
+#define LRM_GEMM_FORCE_SIMT 1  /* CUDA-core kernels for bf16 too (fp32 accumulation)               */
+
+/* Text for a status code (static storage, never NULL). */
+const char* lrm_status_string(lrm_status s);
+
+/*
+ * Bytes of scratch `ws` that lrm_select and lrm_grouped_backward need for these sizes (one
+ * buffer serves both; calls on one stream may share it).  Writes *bytes.  Host-only, no GPU
+ * work.  Errors: LRM_ERR_INVALID_ARG (bytes NULL, negative size), LRM_ERR_SHAPE, LRM_ERR_DTYPE.
+ */
+lrm_status lrm_workspace_size(int64_t T, int32_t k, int32_t E, int32_t H, int32_t I, lrm_dtype dt,
+                              size_t* bytes);
+
+/*
+ * Per-expert loads and backward retention quotas, fixed before the expert forward and
+ * constant for the layer call ("Backward demand is not a constant"; the Portuguese list's
+ * second step).  The articles' controller derives them from memory and network state; this
+ * entry point applies one of the fixed rules of lrm_quota_kind.
+ *   topk_idx [T*k] int32    expert id of each pair (ids outside [0,E) are counted nowhere and
+ *                           set LRM_ERR_BAD_INDEX in dev_status)
+ *   explicit_quotas [E]     int32, read only for LRM_QUOTA_EXPLICIT (may be NULL otherwise)
+ *   loads [E], quotas [E]   int32 outputs
+ * num > 0, den > 0 for RATIO; cap >= 0 for CAP.  Launches a memset and two small kernels.
+ */
+lrm_status lrm_plan_quotas(const int32_t* topk_idx, int64_t T, int32_t k, int32_t E, lrm_quota_kind kind,
+                           int32_t num, int32_t den, int32_t cap, const int32_t* explicit_quotas,
+                           int32_t* loads, int32_t* quotas, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * LRM score of every pair ("LRM: a decomposable contribution score"):
+ *   R_u = alpha_u^2 * ||g_t||_2^2 * ||phi_u||_2^2  (= ||(alpha_u g_t) phi_u^T||_F^2),
+ * accumulated and returned in fp32.
+ *   alpha [T*k] fp32, g [T,H] dt, phi [T*k, I] dt  ->  scores [T*k] fp32.
+ * A non-finite score sets LRM_ERR_NONFINITE in dev_status (the score is still written).
+ */
+lrm_status lrm_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H,
+                     int32_t I, lrm_dtype dt, float* scores, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Keep each expert's top-quota pairs (Portuguese list, step "Seleção pela métrica LRM": inside
+ * the quota the highest-scoring pairs stay).  Expert e keeps min(max(quota_e,0), load_e) pairs:
+ * largest score first, equal scores to the smaller pair index u.
+ *   topk_idx [T*k] int32, scores [T*k] fp32 (finite, >= 0), quotas [E] int32
+ *   seg_offsets [E+1] int32   out: exclusive prefix sum of kept counts (segment e = rows
+ *                             seg_offsets[e] .. seg_offsets[e+1]-1)
+ *   kept_pair [cap] int32     out: kept pair indices, expert-major, u ascending in a segment
+ *   row_of_pair [T*k] int32   out: compacted row of each pair, -1 if dropped
+ *   cap                       rows available in kept_pair (and in the compacted buffers later);
+ *                             if the kept total exceeds it, LRM_ERR_CAPACITY is set and nothing
+ *                             is kept (seg_offsets all 0, row_of_pair all -1).  cap = T*k
+ *                             always suffices.
+ *   ws, ws_bytes              scratch of at least lrm_workspace_size bytes
+ * Deterministic: the output does not depend on scheduling.
+ */
+lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t T,
+                      int32_t k, int32_t E, int64_t cap, int32_t* seg_offsets, int32_t* kept_pair,
+                      int32_t* row_of_pair, void* ws, size_t ws_bytes, int32_t* dev_status,
+                      cudaStream_t stream);
+
+/*
+ * Physical compaction ("The part that is easy to get wrong": retained gradient rows and their
+ * saved activations repacked into contiguous expert-specific buffers, no padding).  For every
+ * kept pair u = t*k + j with r = row_of_pair[u] >= 0:
+ *   dy_c[r] = round_dt(alpha_u * g_t)   (fp32 product, round to nearest even)
+ *   x_c[r] = x_t,   h_c[r] = h_u,   phi_c[r] = phi_u
+ *   row_of_pair [T*k] int32 (from lrm_select), alpha [T*k] fp32, g [T,H], x [T,H],
+ *   h [T*k, 2I], phi [T*k, I]  ->  dy_c [cap,H], x_c [cap,H], h_c [cap,2I], phi_c [cap,I] (dt).
+ * Rows are visited token by token, so g_t and x_t are read once per token.  Rows >= cap are
+ * skipped.
+ */
+lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x,
+                       const void* h, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
+                       lrm_dtype dt, int64_t cap, void* dy_c, void* x_c, void* h_c, void* phi_c,
+                       cudaStream_t stream);
+
+/*
+ * SwiGLU expert backward as variable-size grouped GEMMs driven by the retained row counts
+ * ("The part that is easy to get wrong"; the Portuguese list's compaction step).  For each
+ * expert e over its segment (R_e rows, read on the device from seg_offsets; no host sync):
+ *   dw_down[e]    = dy_c[e]^T phi_c[e]                               [E,H,I]  fp32, overwritten
+ *   dphi          = dy_c[e] w_down[e]; s = sigmoid(gate)
+ *   dh_c[e]       = [dphi*up*s*(1+gate*(1-s)) ; dphi*gate*s]         [cap,2I] dt
+ *   dw_gate_up[e] = dh_c[e]^T x_c[e]                                 [E,2I,H] fp32, overwritten
+ *   dx_c[e]       = dh_c[e] w_gate_up[e]                             [cap,H]  dt
+ * An expert with R_e = 0 gets dw = 0 exactly.  w_gate_up [E,2I,H] (gate rows first),
+ * w_down [E,H,I].  Accumulation is fp32.  `flags` is LRM_GEMM_DEFAULT or LRM_GEMM_FORCE_SIMT.
+ * seg_offsets must be non-decreasing with seg_offsets[E] <= cap (as lrm_select writes them).
+ * Errors: host as usual; LRM_ERR_UNSUPPORTED when the tensor-core kernels are requested on a
+ * device that is not sm_103; device LRM_ERR_TIMEOUT if a pipeline wait gives up (the kernel
+ * then returns early and its outputs are incomplete).
+ */
+lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
+                                const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E,
+                                int32_t H, int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up,
+                                float* dw_down, void* dh_c, void* dx_c, void* ws, size_t ws_bytes,
+                                int32_t flags, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Back to the original token layout (Portuguese list: "the result returns to the original
+ * layout"):  dx[t] = sum over j = 0..k-1, in that order, of dx_c[row_of_pair[t*k+j]] for kept
+ * pairs, summed in fp32 and rounded once to dt; a token with no kept pair gets 0.  No atomics:
+ * the result is deterministic.
+ *   row_of_pair [T*k] int32, dx_c [cap,H] dt  ->  dx [T,H] dt.
+ */
+lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,
+                          lrm_dtype dt, void* dx, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LRM_H */

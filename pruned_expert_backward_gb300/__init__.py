@@ -1,0 +1,7 @@
+"""LRM-pruned MoE expert backward on one GB300 (sm_103a): C ABI (include/lrm.h) + Python binding.
+
+Importing the package does not load the library; the first call does, and raises if
+liblrm.so has not been built (python -m pruned_expert_backward_gb300.build).
+"""
+from .api import (LrmError, PrunedBackward, lrm_compact, lrm_grouped_backward, lrm_plan_quotas,  # noqa: F401
+                  lrm_scatter_dx, lrm_score, lrm_select, lrm_workspace_size)

@@ -1,0 +1,203 @@
+"""Python binding of include/lrm.h: the same entry points, taking torch CUDA tensors.
+
+Argument marshalling only (shapes, dtypes, pointers, the current stream); every step of
+the pruned backward runs in liblrm.so's kernels.  There is no CPU path: a missing
+library, a CPU tensor or a failed status raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+
+import torch
+
+from . import _lib as L
+
+
+class LrmError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        name = L.STATUS_NAMES.get(code, str(code))
+        text = L.load().lrm_status_string(code).decode()
+        super().__init__(f"{where}: {name} ({text})")
+
+
+def _ok(code: int, where: str):
+    if code != L.LRM_OK:
+        raise LrmError(code, where)
+
+
+def _dt(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return L.LRM_BF16
+    if t.dtype == torch.float32:
+        return L.LRM_F32
+    raise TypeError(f"unsupported dtype {t.dtype}: bf16 or fp32")
+
+
+def _cuda(t: torch.Tensor, name: str, dtype=None) -> int:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _opt(t, name, dtype=None):
+    return None if t is None else _cuda(t, name, dtype)
+
+
+def _stream() -> int:
+    return torch.cuda.current_stream().cuda_stream
+
+
+def lrm_workspace_size(T: int, k: int, E: int, H: int, I: int, dtype: torch.dtype) -> int:
+    out = C.c_size_t(0)
+    dt = L.LRM_BF16 if dtype == torch.bfloat16 else L.LRM_F32
+    _ok(L.load().lrm_workspace_size(T, k, E, H, I, dt, C.byref(out)), "lrm_workspace_size")
+    return int(out.value)
+
+
+def lrm_plan_quotas(topk_idx, E, kind, num=0, den=1, cap=0, explicit=None, loads=None, quotas=None,
+                    dev_status=None):
+    """kind: "ratio" (num/den), "cap" (cap) or "explicit" (explicit int32 [E] tensor)."""
+    T, k = topk_idx.shape
+    dev = topk_idx.device
+    loads = torch.empty(E, dtype=torch.int32, device=dev) if loads is None else loads
+    quotas = torch.empty(E, dtype=torch.int32, device=dev) if quotas is None else quotas
+    kinds = {"ratio": L.LRM_QUOTA_RATIO, "cap": L.LRM_QUOTA_CAP, "explicit": L.LRM_QUOTA_EXPLICIT}
+    _ok(L.load().lrm_plan_quotas(_cuda(topk_idx, "topk_idx", torch.int32), T, k, E, kinds[kind], num, den, cap,
+                                 _opt(explicit, "explicit", torch.int32), _cuda(loads, "loads", torch.int32),
+                                 _cuda(quotas, "quotas", torch.int32), _opt(dev_status, "dev_status", torch.int32),
+                                 _stream()), "lrm_plan_quotas")
+    return loads, quotas
+
+
+def lrm_score(alpha, g, phi, scores=None, dev_status=None):
+    T, H = g.shape
+    k, I = phi.shape[-2], phi.shape[-1]
+    if phi.numel() != T * k * I or alpha.numel() != T * k:
+        raise ValueError("alpha [T,k], g [T,H], phi [T,k,I] expected")
+    scores = torch.empty(T * k, dtype=torch.float32, device=g.device) if scores is None else scores
+    _ok(L.load().lrm_score(_cuda(alpha, "alpha", torch.float32), _cuda(g, "g"), _cuda(phi, "phi", g.dtype), T, k,
+                           H, I, _dt(g), _cuda(scores, "scores", torch.float32),
+                           _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_score")
+    return scores
+
+
+def lrm_select(topk_idx, scores, quotas, E, cap=None, seg_offsets=None, kept_pair=None, row_of_pair=None,
+               ws=None, dev_status=None):
+    T, k = topk_idx.shape
+    P = T * k
+    dev = topk_idx.device
+    cap = P if cap is None else int(cap)
+    seg_offsets = torch.empty(E + 1, dtype=torch.int32, device=dev) if seg_offsets is None else seg_offsets
+    kept_pair = torch.empty(max(cap, 1), dtype=torch.int32, device=dev) if kept_pair is None else kept_pair
+    row_of_pair = torch.empty(P, dtype=torch.int32, device=dev) if row_of_pair is None else row_of_pair
+    if ws is None:
+        ws = torch.empty(lrm_workspace_size(T, k, E, 8, 8, torch.float32), dtype=torch.uint8, device=dev)
+    _ok(L.load().lrm_select(_cuda(topk_idx, "topk_idx", torch.int32), _cuda(scores, "scores", torch.float32),
+                            _cuda(quotas, "quotas", torch.int32), T, k, E, cap,
+                            _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(kept_pair, "kept_pair", torch.int32),
+                            _cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(ws, "ws"), ws.numel(),
+                            _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_select")
+    return seg_offsets, kept_pair, row_of_pair
+
+
+def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=None, phi_c=None):
+    T, H = g.shape
+    k, I = phi.shape[-2], phi.shape[-1]
+    dev, dt = g.device, g.dtype
+    rows = max(int(cap), 1)
+    dy_c = torch.empty(rows, H, dtype=dt, device=dev) if dy_c is None else dy_c
+    x_c = torch.empty(rows, H, dtype=dt, device=dev) if x_c is None else x_c
+    h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
+    phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
+    _ok(L.load().lrm_compact(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(alpha, "alpha", torch.float32),
+                             _cuda(g, "g"), _cuda(x, "x", dt), _cuda(h, "h", dt), _cuda(phi, "phi", dt), T, k, H, I,
+                             _dt(g), int(cap), _cuda(dy_c, "dy_c", dt), _cuda(x_c, "x_c", dt),
+                             _cuda(h_c, "h_c", dt), _cuda(phi_c, "phi_c", dt), _stream()), "lrm_compact")
+    return dy_c, x_c, h_c, phi_c
+
+
+def lrm_grouped_backward(seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, cap, dw_gate_up=None,
+                         dw_down=None, dh_c=None, dx_c=None, ws=None, flags=L.LRM_GEMM_DEFAULT, dev_status=None):
+    E, H, I = w_down.shape
+    dev, dt = w_down.device, w_down.dtype
+    rows = max(int(cap), 1)
+    dw_gate_up = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev) if dw_gate_up is None else dw_gate_up
+    dw_down = torch.empty(E, H, I, dtype=torch.float32, device=dev) if dw_down is None else dw_down
+    dh_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if dh_c is None else dh_c
+    dx_c = torch.empty(rows, H, dtype=dt, device=dev) if dx_c is None else dx_c
+    if ws is None:
+        ws = torch.empty(lrm_workspace_size(0, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
+    _ok(L.load().lrm_grouped_backward(
+        _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(dy_c, "dy_c", dt), _cuda(x_c, "x_c", dt),
+        _cuda(h_c, "h_c", dt), _cuda(phi_c, "phi_c", dt), _cuda(w_gate_up, "w_gate_up", dt),
+        _cuda(w_down, "w_down", dt), E, H, I, _dt(w_down), int(cap),
+        _cuda(dw_gate_up, "dw_gate_up", torch.float32), _cuda(dw_down, "dw_down", torch.float32),
+        _cuda(dh_c, "dh_c", dt), _cuda(dx_c, "dx_c", dt), _cuda(ws, "ws"), ws.numel(), int(flags),
+        _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_grouped_backward")
+    return dw_gate_up, dw_down, dh_c, dx_c
+
+
+def lrm_scatter_dx(row_of_pair, dx_c, T, k, dx=None):
+    H = dx_c.shape[1]
+    dx = torch.empty(T, H, dtype=dx_c.dtype, device=dx_c.device) if dx is None else dx
+    _ok(L.load().lrm_scatter_dx(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(dx_c, "dx_c"), T, k, H,
+                                _dt(dx_c), _cuda(dx, "dx", dx_c.dtype), _stream()), "lrm_scatter_dx")
+    return dx
+
+
+class PrunedBackward:
+    """The whole pruned expert backward for one fixed problem size, with every buffer
+    allocated once (device memory from torch).  `run` queues score -> select -> compact ->
+    grouped backward -> scatter on the current stream; no host synchronisation.
+
+    cap defaults to T*k, which can never overflow; a caller that knows sum(min(quota, load))
+    may pass it to shrink the compacted buffers."""
+
+    def __init__(self, T, k, E, H, I, dtype=torch.bfloat16, device="cuda", cap=None, flags=L.LRM_GEMM_DEFAULT):
+        self.T, self.k, self.E, self.H, self.I = T, k, E, H, I
+        self.dtype, self.flags = dtype, flags
+        self.cap = T * k if cap is None else int(cap)
+        dev = torch.device(device)
+        rows = max(self.cap, 1)
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.scores = torch.empty(T * k, dtype=torch.float32, device=dev)
+        self.seg_offsets = torch.empty(E + 1, **i32)
+        self.kept_pair = torch.empty(rows, **i32)
+        self.row_of_pair = torch.empty(max(T * k, 1), **i32)
+        self.dy_c = torch.empty(rows, H, dtype=dtype, device=dev)
+        self.x_c = torch.empty(rows, H, dtype=dtype, device=dev)
+        self.h_c = torch.empty(rows, 2 * I, dtype=dtype, device=dev)
+        self.phi_c = torch.empty(rows, I, dtype=dtype, device=dev)
+        self.dh_c = torch.empty(rows, 2 * I, dtype=dtype, device=dev)
+        self.dx_c = torch.empty(rows, H, dtype=dtype, device=dev)
+        self.dw_gate_up = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev)
+        self.dw_down = torch.empty(E, H, I, dtype=torch.float32, device=dev)
+        self.dx = torch.empty(T, H, dtype=dtype, device=dev)
+        self.ws = torch.empty(lrm_workspace_size(T, k, E, H, I, dtype), dtype=torch.uint8, device=dev)
+        self.dev_status = torch.zeros(1, **i32)
+
+    def run(self, inp, quotas):
+        """inp: dict with topk_idx [T,k] int32, alpha [T,k] fp32, x, g [T,H], h [T,k,2I], phi [T,k,I],
+        w_gate_up [E,2I,H], w_down [E,H,I] (CUDA).  quotas: int32 [E] (CUDA)."""
+        lrm_score(inp["alpha"], inp["g"], inp["phi"], scores=self.scores, dev_status=self.dev_status)
+        lrm_select(inp["topk_idx"], self.scores, quotas, self.E, cap=self.cap, seg_offsets=self.seg_offsets,
+                   kept_pair=self.kept_pair, row_of_pair=self.row_of_pair, ws=self.ws, dev_status=self.dev_status)
+        lrm_compact(self.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], self.cap,
+                    dy_c=self.dy_c, x_c=self.x_c, h_c=self.h_c, phi_c=self.phi_c)
+        lrm_grouped_backward(self.seg_offsets, self.dy_c, self.x_c, self.h_c, self.phi_c, inp["w_gate_up"],
+                             inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
+                             dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
+                             dev_status=self.dev_status)
+        lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx)
+        return self
+
+    def outputs(self):
+        return {"scores": self.scores, "seg_offsets": self.seg_offsets, "kept_pair": self.kept_pair,
+                "row_of_pair": self.row_of_pair, "dy_c": self.dy_c, "x_c": self.x_c, "h_c": self.h_c,
+                "phi_c": self.phi_c, "dh_c": self.dh_c, "dx_c": self.dx_c, "dw_gate_up": self.dw_gate_up,
+                "dw_down": self.dw_down, "dx": self.dx, "dev_status": self.dev_status}

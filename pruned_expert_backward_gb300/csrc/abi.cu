@@ -1,0 +1,191 @@
+// C ABI of the LRM-pruned expert backward: argument validation, workspace layout, dispatch.
+// Every entry point only queues work on the caller's stream; nothing here allocates or
+// synchronises.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lrm {
+
+namespace {
+
+constexpr size_t kAlign = 256;
+size_t up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+bool al16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+lrm_status check_dims(int64_t T, int32_t k, int32_t E, int32_t H, int32_t I) {
+  if (T < 0 || k < 1 || E < 1 || H < 1 || I < 1) return LRM_ERR_INVALID_ARG;
+  if (k > LRM_MAX_TOPK || E > LRM_MAX_EXPERTS) return LRM_ERR_SHAPE;
+  if (H % 8 != 0 || I % 8 != 0) return LRM_ERR_SHAPE;
+  if (T * (int64_t)k > INT32_MAX) return LRM_ERR_SHAPE;
+  return LRM_OK;
+}
+lrm_status check_dt(lrm_dtype dt) { return (dt == LRM_BF16 || dt == LRM_F32) ? LRM_OK : LRM_ERR_DTYPE; }
+
+lrm_status after_launch() {
+  const cudaError_t e = cudaGetLastError();
+  return e == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
+}
+
+}  // namespace
+
+WsLayout workspace_layout(int64_t P, int32_t E) {
+  WsLayout w{};
+  const int64_t nc = (P + kSelChunk - 1) / kSelChunk;
+  size_t off = 0;
+  w.counts = off;       off += up(sizeof(int32_t) * (size_t)(nc > 0 ? nc : 1) * E);
+  w.bucket_start = off; off += up(sizeof(int32_t) * (size_t)(E + 1));
+  w.keep = off;         off += up(sizeof(int32_t) * (size_t)E);
+  w.sorted_u = off;     off += up(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
+  w.sorted_key = off;   off += up(sizeof(uint32_t) * (size_t)(P > 0 ? P : 1));
+  w.gemm = off;         off += up(4096);
+  w.total = off;
+  return w;
+}
+
+}  // namespace lrm
+
+using namespace lrm;
+
+extern "C" {
+
+const char* lrm_status_string(lrm_status s) {
+  switch (s) {
+    case LRM_OK: return "ok";
+    case LRM_ERR_INVALID_ARG: return "invalid argument (null/misaligned pointer, negative size or bad enum)";
+    case LRM_ERR_SHAPE: return "size outside the supported limits";
+    case LRM_ERR_DTYPE: return "unknown dtype";
+    case LRM_ERR_WORKSPACE: return "workspace missing or too small";
+    case LRM_ERR_CUDA: return "CUDA launch or runtime error";
+    case LRM_ERR_CAPACITY: return "kept rows exceed the capacity";
+    case LRM_ERR_NONFINITE: return "non-finite score";
+    case LRM_ERR_TIMEOUT: return "a bounded device wait gave up";
+    case LRM_ERR_BAD_INDEX: return "expert id outside [0, E)";
+    case LRM_ERR_UNSUPPORTED: return "unsupported device or configuration";
+  }
+  return "unknown status";
+}
+
+lrm_status lrm_workspace_size(int64_t T, int32_t k, int32_t E, int32_t H, int32_t I, lrm_dtype dt, size_t* bytes) {
+  if (!bytes) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_dims(T, k, E, H, I);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  *bytes = workspace_layout(T * k, E).total;
+  return LRM_OK;
+}
+
+lrm_status lrm_plan_quotas(const int32_t* topk_idx, int64_t T, int32_t k, int32_t E, lrm_quota_kind kind,
+                           int32_t num, int32_t den, int32_t cap, const int32_t* explicit_quotas, int32_t* loads,
+                           int32_t* quotas, int32_t* dev_status, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, E, 8, 8);
+  if (st) return st;
+  if ((T > 0 && !topk_idx) || !loads || !quotas) return LRM_ERR_INVALID_ARG;
+  if (kind == LRM_QUOTA_RATIO) {
+    if (num <= 0 || den <= 0) return LRM_ERR_INVALID_ARG;
+  } else if (kind == LRM_QUOTA_CAP) {
+    if (cap < 0) return LRM_ERR_INVALID_ARG;
+  } else if (kind == LRM_QUOTA_EXPLICIT) {
+    if (!explicit_quotas) return LRM_ERR_INVALID_ARG;
+  } else {
+    return LRM_ERR_INVALID_ARG;
+  }
+  launch_plan_quotas(topk_idx, T * k, E, (int)kind, num, den, cap, explicit_quotas, loads, quotas, dev_status, stream);
+  return after_launch();
+}
+
+lrm_status lrm_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
+                     lrm_dtype dt, float* scores, int32_t* dev_status, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, 1, H, I);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (T > 0 && (!alpha || !g || !phi || !scores)) return LRM_ERR_INVALID_ARG;
+  if (!al16(g) || !al16(phi)) return LRM_ERR_INVALID_ARG;
+  launch_score(alpha, g, phi, T, k, H, I, dt, scores, dev_status, stream);
+  return after_launch();
+}
+
+lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t T, int32_t k,
+                      int32_t E, int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair,
+                      void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, E, 8, 8);
+  if (st) return st;
+  const int64_t P = T * k;
+  if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
+  if (!quotas || !seg_offsets) return LRM_ERR_INVALID_ARG;
+  if (P > 0 && (!topk_idx || !scores || !row_of_pair)) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && !kept_pair) return LRM_ERR_INVALID_ARG;
+  const WsLayout w = workspace_layout(P, E);
+  if (!ws || ws_bytes < w.total) return LRM_ERR_WORKSPACE;
+  char* b = static_cast<char*>(ws);
+  SelectWs sw;
+  sw.counts = reinterpret_cast<int32_t*>(b + w.counts);
+  sw.bucket_start = reinterpret_cast<int32_t*>(b + w.bucket_start);
+  sw.keep = reinterpret_cast<int32_t*>(b + w.keep);
+  sw.sorted_u = reinterpret_cast<int32_t*>(b + w.sorted_u);
+  sw.sorted_key = reinterpret_cast<uint32_t*>(b + w.sorted_key);
+  sw.n_chunks = (P + kSelChunk - 1) / kSelChunk;
+  launch_select(topk_idx, scores, quotas, P, E, cap, seg_offsets, kept_pair, row_of_pair, sw, dev_status, stream);
+  return after_launch();
+}
+
+lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x, const void* h,
+                       const void* phi, int64_t T, int32_t k, int32_t H, int32_t I, lrm_dtype dt, int64_t cap,
+                       void* dy_c, void* x_c, void* h_c, void* phi_c, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, 1, H, I);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
+  if (T > 0 && (!row_of_pair || !alpha || !g || !x || !h || !phi)) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && (!dy_c || !x_c || !h_c || !phi_c)) return LRM_ERR_INVALID_ARG;
+  const void* ptrs[] = {g, x, h, phi, dy_c, x_c, h_c, phi_c};
+  for (const void* p : ptrs)
+    if (!al16(p)) return LRM_ERR_INVALID_ARG;
+  launch_compact(row_of_pair, alpha, g, x, h, phi, T, k, H, I, dt, cap, dy_c, x_c, h_c, phi_c, stream);
+  return after_launch();
+}
+
+lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
+                                const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E, int32_t H,
+                                int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
+                                void* dx_c, void* ws, size_t ws_bytes, int32_t flags, int32_t* dev_status,
+                                cudaStream_t stream) {
+  lrm_status st = check_dims(0, 1, E, H, I);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
+  if (flags != LRM_GEMM_DEFAULT && flags != LRM_GEMM_FORCE_SIMT) return LRM_ERR_INVALID_ARG;
+  if (!seg_offsets || !w_gate_up || !w_down || !dw_gate_up || !dw_down) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && (!dy_c || !x_c || !h_c || !phi_c || !dh_c || !dx_c)) return LRM_ERR_INVALID_ARG;
+  const void* ptrs[] = {dy_c, x_c, h_c, phi_c, w_gate_up, w_down, dw_gate_up, dw_down, dh_c, dx_c};
+  for (const void* p : ptrs)
+    if (!al16(p)) return LRM_ERR_INVALID_ARG;
+  if (!ws) return LRM_ERR_WORKSPACE;
+  GroupedArgs a{seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, E, H, I, cap,
+                dw_gate_up, dw_down, dh_c, dx_c, dev_status};
+  if (dt == LRM_BF16 && flags == LRM_GEMM_DEFAULT) {
+    // workspace: the tensor-core path keeps its tile tables (2E+1 ints) at the start
+    if (ws_bytes < up(sizeof(int32_t) * (2 * (size_t)E + 1))) return LRM_ERR_WORKSPACE;
+    GemmWs gw;
+    gw.tile_counter = static_cast<int32_t*>(ws);
+    gw.tmaps = nullptr;
+    return launch_grouped_tc(a, gw, stream);
+  }
+  launch_grouped_simt(a, dt, stream);
+  return after_launch();
+}
+
+lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,
+                          lrm_dtype dt, void* dx, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, 1, H, 8);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (T > 0 && (!row_of_pair || !dx_c || !dx)) return LRM_ERR_INVALID_ARG;
+  if (!al16(dx_c) || !al16(dx)) return LRM_ERR_INVALID_ARG;
+  launch_scatter_dx(row_of_pair, dx_c, T, k, H, dt, dx, stream);
+  return after_launch();
+}
+
+}  // extern "C"

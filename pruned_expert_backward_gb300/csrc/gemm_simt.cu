@@ -1,0 +1,218 @@
+// CUDA-core grouped GEMMs of the SwiGLU expert backward (fp32 accumulation).
+//
+// Used for fp32 inputs, where tensor-core formats (TF32/BF16) would not reach fp32
+// accuracy, and on request for bf16.  Segment sizes are read on the device from
+// seg_offsets, so nothing waits on the host ("LRMoE: Trimming Backward Work in
+// Memory-Bound MoE Training", section "The part that is easy to get wrong": the actual
+// retained row counts drive variable-size grouped GEMMs, with no padding).
+//
+//  var-M (rows of a segment are the M dimension):
+//    dphi = dy_c[e] W_down[e]  with the SwiGLU backward fused into the epilogue -> dh_c
+//    dx_c = dh_c[e] W_gate_up[e]
+//  var-K (rows of a segment are the reduction dimension):
+//    dW_down[e] = dy_c[e]^T phi_c[e],  dW_gate_up[e] = dh_c[e]^T x_c[e]
+// 64 x 64 output tiles, 16-deep K slices in shared memory, 256 threads x 4 x 4 outputs.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lrm {
+
+namespace {
+
+constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
+
+enum { EPI_SWIGLU = 0, EPI_STORE = 1 };
+
+// Map a virtual M-tile id to (expert, first row, end row) from the per-expert tile prefix.
+__device__ __forceinline__ bool find_mtile(const int32_t* seg, int E, int vt, int* s_prefix, int* e_out,
+                                           int* r0_out, int* r1_out) {
+  // s_prefix[e] = number of M tiles of experts < e (computed by the caller's block).
+  int lo = 0, hi = E;  // find largest e with s_prefix[e] <= vt
+  if (vt >= s_prefix[E]) return false;
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (s_prefix[mid] <= vt) lo = mid; else hi = mid;
+  }
+  const int e = lo;
+  const int r0 = seg[e] + (vt - s_prefix[e]) * BM;
+  *e_out = e;
+  *r0_out = r0;
+  *r1_out = min(seg[e + 1], r0 + BM);
+  return true;
+}
+
+__device__ void mtile_prefix(const int32_t* seg, int E, int* s_prefix) {
+  // serial prefix by thread 0 is fine: E <= 1024 and this kernel is the fallback path
+  if (threadIdx.x == 0) {
+    int acc = 0;
+    for (int e = 0; e < E; ++e) {
+      s_prefix[e] = acc;
+      acc += (seg[e + 1] - seg[e] + BM - 1) / BM;
+    }
+    s_prefix[E] = acc;
+  }
+  __syncthreads();
+}
+
+// C[r, n] = sum_k A[r, k] * B_e[k, n]; A [rows, K] row-major, B_e [K, N] row-major.
+template <typename T, int EPI>
+__global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ seg, int E,
+                                                  const T* __restrict__ A, const T* __restrict__ B, int K, int N,
+                                                  const T* __restrict__ h_c, T* __restrict__ out) {
+  __shared__ int s_prefix[LRM_MAX_EXPERTS + 1];
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  mtile_prefix(seg, E, s_prefix);
+  int e, r0, r1;
+  if (!find_mtile(seg, E, blockIdx.x, s_prefix, &e, &r0, &r1)) return;
+  const int n0 = blockIdx.y * BN;
+  const T* Be = B + (int64_t)e * K * N;
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < K; k0 += BK) {
+    // A tile: 64 rows x 16 k; thread loads 4 consecutive k of one row
+    {
+      const int m = threadIdx.x / 4, kq = (threadIdx.x % 4) * 4;
+      const int r = r0 + m;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int kk = k0 + kq + q;
+        As[kq + q][m] = (r < r1 && kk < K) ? to_f(A[(int64_t)r * K + kk]) : 0.f;
+      }
+    }
+    // B tile: 16 k x 64 n
+    {
+      const int kk = threadIdx.x / 16, nq = (threadIdx.x % 16) * 4;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int n = n0 + nq + q;
+        Bs[kk][nq + q] = (k0 + kk < K && n < N) ? to_f(Be[(int64_t)(k0 + kk) * N + n]) : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int r = r0 + ty * 4 + i;
+    if (r >= r1) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n >= N) continue;
+      if (EPI == EPI_SWIGLU) {
+        // N = I here; h_c row is [gate (I) ; up (I)]
+        const float gate = to_f(h_c[(int64_t)r * 2 * N + n]);
+        const float up = to_f(h_c[(int64_t)r * 2 * N + N + n]);
+        const float sg = 1.f / (1.f + expf(-gate));
+        const float dphi = acc[i][j];
+        out[(int64_t)r * 2 * N + n] = from_f<T>(dphi * up * sg * (1.f + gate * (1.f - sg)));
+        out[(int64_t)r * 2 * N + N + n] = from_f<T>(dphi * gate * sg);
+      } else {
+        out[(int64_t)r * N + n] = from_f<T>(acc[i][j]);
+      }
+    }
+  }
+}
+
+// C_e[m, n] = sum_{r in segment e} A[r, m] * B[r, n]; A [rows, M], B [rows, N] row-major.
+template <typename T>
+__global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ seg, const T* __restrict__ A,
+                                                  const T* __restrict__ B, int M, int N, float* __restrict__ C) {
+  __shared__ float As[BK][BM + 4];
+  __shared__ float Bs[BK][BN + 4];
+  const int e = blockIdx.z;
+  const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
+  const int r0 = seg[e], r1 = seg[e + 1];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  float acc[4][4] = {};
+  for (int k0 = r0; k0 < r1; k0 += BK) {
+    {
+      const int kk = threadIdx.x / 16, q4 = (threadIdx.x % 16) * 4;
+      const int r = k0 + kk;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int m = m0 + q4 + q, n = n0 + q4 + q;
+        As[kk][q4 + q] = (r < r1 && m < M) ? to_f(A[(int64_t)r * M + m]) : 0.f;
+        Bs[kk][q4 + q] = (r < r1 && n < N) ? to_f(B[(int64_t)r * N + n]) : 0.f;
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < BK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty * 4 + i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx * 4 + j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+  float* Ce = C + (int64_t)e * M * N;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty * 4 + i;
+    if (m >= M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx * 4 + j;
+      if (n < N) Ce[(int64_t)m * N + n] = acc[i][j];
+    }
+  }
+}
+
+template <typename T>
+void run_all(const GroupedArgs& a, cudaStream_t s) {
+  const int E = a.E, H = a.H, I = a.I;
+  // Upper bound on M tiles: every expert adds at most one partial tile.
+  const int64_t mtiles = (a.cap + BM - 1) / BM + E;
+  const T* dy = (const T*)a.dy_c;
+  const T* xc = (const T*)a.x_c;
+  const T* hc = (const T*)a.h_c;
+  const T* pc = (const T*)a.phi_c;
+  T* dh = (T*)a.dh_c;
+  T* dx = (T*)a.dx_c;
+  if (mtiles > 0) {
+    // dphi + SwiGLU backward: [R_e, H] x [H, I]
+    varm_kernel<T, EPI_SWIGLU><<<dim3((unsigned)mtiles, (I + BN - 1) / BN), NT, 0, s>>>(
+        a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh);
+  }
+  // dW_down[e] = dy_c^T phi_c : [H, I]
+  vark_kernel<T><<<dim3((I + BN - 1) / BN, (H + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, dy, pc, H, I,
+                                                                              a.dw_down);
+  // dW_gate_up[e] = dh_c^T x_c : [2I, H]
+  vark_kernel<T><<<dim3((H + BN - 1) / BN, (2 * I + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, (const T*)dh, xc,
+                                                                                  2 * I, H, a.dw_gate_up);
+  if (mtiles > 0) {
+    // dx_c = dh_c W_gate_up[e] : [R_e, 2I] x [2I, H]
+    varm_kernel<T, EPI_STORE><<<dim3((unsigned)mtiles, (H + BN - 1) / BN), NT, 0, s>>>(
+        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx);
+  }
+}
+
+}  // namespace
+
+void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s) {
+  if (dt == LRM_BF16)
+    run_all<__nv_bfloat16>(a, s);
+  else
+    run_all<float>(a, s);
+}
+
+}  // namespace lrm

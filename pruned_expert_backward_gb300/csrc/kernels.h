@@ -1,0 +1,68 @@
+// Internal launchers of the LRM-pruned expert backward kernels.  abi.cu validates the
+// arguments of the public entry points and calls these; they only launch.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "lrm.h"
+
+namespace lrm {
+
+// Selection works on warp-sized chunks of this many consecutive pairs.
+constexpr int kSelChunk = 2048;
+constexpr int kSelWarpsPerBlock = 8;
+
+struct SelectWs {
+  int32_t* counts;        // [n_chunks][E]  per-chunk expert counts, then exclusive bases
+  int32_t* bucket_start;  // [E+1]          start of each expert's bucket in sorted_u
+  int32_t* keep;          // [E]            min(max(quota,0), load), or 0 on capacity overflow
+  int32_t* sorted_u;      // [P]            pairs grouped by expert, u ascending
+  uint32_t* sorted_key;   // [P]            score bits in the same order
+  int64_t n_chunks;
+};
+
+struct GemmWs {
+  int32_t* tile_counter;  // [4] dynamic tile queues (zeroed by the launcher)
+  void* tmaps;            // reserved
+};
+
+struct WsLayout {
+  size_t counts, bucket_start, keep, sorted_u, sorted_key, gemm, total;
+};
+WsLayout workspace_layout(int64_t P, int32_t E);
+
+void launch_plan_quotas(const int32_t* topk_idx, int64_t P, int32_t E, int kind, int32_t num, int32_t den,
+                        int32_t cap, const int32_t* explicit_q, int32_t* loads, int32_t* quotas, int32_t* status,
+                        cudaStream_t s);
+
+void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
+                  lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s);
+
+void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t P, int32_t E,
+                   int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair, const SelectWs& ws,
+                   int32_t* status, cudaStream_t s);
+
+void launch_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x, const void* h,
+                    const void* phi, int64_t T, int32_t k, int32_t H, int32_t I, lrm_dtype dt, int64_t cap,
+                    void* dy_c, void* x_c, void* h_c, void* phi_c, cudaStream_t s);
+
+void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H, lrm_dtype dt,
+                       void* dx, cudaStream_t s);
+
+struct GroupedArgs {
+  const int32_t* seg_offsets;
+  const void *dy_c, *x_c, *h_c, *phi_c, *w_gate_up, *w_down;
+  int32_t E, H, I;
+  int64_t cap;
+  float *dw_gate_up, *dw_down;
+  void *dh_c, *dx_c;
+  int32_t* status;
+};
+
+void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s);
+// Returns LRM_OK, or LRM_ERR_UNSUPPORTED / LRM_ERR_CUDA when the tensor-core path cannot run.
+lrm_status launch_grouped_tc(const GroupedArgs& a, const GemmWs& ws, cudaStream_t s);
+
+}  // namespace lrm

@@ -1,0 +1,283 @@
+// Per-expert top-quota selection.
+//
+// "LRMoE poda a passagem reversa do MoE..." (news.hamidun.com), step "Seleção pela métrica
+// LRM": inside each expert's quota the highest-scoring pairs are kept.  Equal scores go to
+// the smaller pair index u; inside a segment the kept pairs are listed in u order.
+//
+// Four launches, all deterministic:
+//  1. count:   each warp owns a chunk of kSelChunk consecutive pairs and counts its experts.
+//  2. scan:    per expert, exclusive scan of the chunk counts (bucket bases), loads, kept
+//              counts min(quota, load) and the segment offsets (capacity checked here).
+//  3. bucket:  stable scatter of the pairs into expert buckets (u ascending) with their
+//              score bits; ranks within a warp come from __match_any_sync.
+//  4. expert:  one CTA per expert: MSD radix select (4 x 8 bits) of the quota-th largest
+//              score in the bucket, then one ordered pass that keeps everything above the
+//              threshold plus the first `need` pairs equal to it, and writes kept_pair and
+//              row_of_pair through a block-wide prefix sum.
+// Scores are finite and >= 0, so their IEEE bit patterns order like their values.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace lrm {
+
+namespace {
+
+// Exclusive block-wide prefix sum of one int per thread (blockDim.x a multiple of 32, <= 1024).
+// `sm` needs 33 ints.  Returns the exclusive prefix; *total receives the block total.
+__device__ __forceinline__ int block_excl_scan(int v, int* total, int* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  int incl = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int y = __shfl_up_sync(0xffffffffu, incl, o);
+    if (lane >= o) incl += y;
+  }
+  if (lane == 31) sm[warp] = incl;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < nw ? sm[lane] : 0;
+    int wi = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      int y = __shfl_up_sync(0xffffffffu, wi, o);
+      if (lane >= o) wi += y;
+    }
+    if (lane < nw) sm[lane] = wi - w;
+    if (lane == 31) sm[32] = wi;
+  }
+  __syncthreads();
+  const int res = sm[warp] + incl - v;
+  *total = sm[32];
+  __syncthreads();
+  return res;
+}
+
+__global__ void __launch_bounds__(256) sel_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                                                        int64_t n_chunks, int32_t* __restrict__ counts,
+                                                        int32_t* status) {
+  extern __shared__ int hist[];  // [kSelWarpsPerBlock][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  int* h = hist + warp * E;
+  for (int e = lane; e < E; e += 32) h[e] = 0;
+  __syncwarp();
+  const int64_t c = (int64_t)blockIdx.x * kSelWarpsPerBlock + warp;
+  if (c >= n_chunks) return;
+  const int64_t u0 = c * kSelChunk, u1 = min(P, u0 + kSelChunk);
+  for (int64_t u = u0 + lane; u < u1; u += 32) {
+    const int e = idx[u];
+    if (e >= 0 && e < E)
+      atomicAdd(&h[e], 1);
+    else
+      set_status(status, LRM_ERR_BAD_INDEX);
+  }
+  __syncwarp();
+  for (int e = lane; e < E; e += 32) counts[c * E + e] = h[e];
+}
+
+__global__ void __launch_bounds__(1024) sel_scan_kernel(int32_t* __restrict__ counts, int64_t n_chunks, int E,
+                                                        const int32_t* __restrict__ quotas, int64_t cap,
+                                                        int32_t* __restrict__ bucket_start, int32_t* __restrict__ keep,
+                                                        int32_t* __restrict__ seg_offsets, int32_t* status) {
+  __shared__ int sm[33];
+  __shared__ int s_overflow;
+  const int e = threadIdx.x;  // E <= 1024 = blockDim.x
+  int load = 0;
+  if (e < E) {
+#pragma unroll 8
+    for (int64_t c = 0; c < n_chunks; ++c) {
+      const int v = counts[c * E + e];
+      counts[c * E + e] = load;
+      load += v;
+    }
+  }
+  int kp = 0;
+  if (e < E) {
+    const int q = quotas[e];
+    kp = q < 0 ? 0 : (q > load ? load : q);
+  }
+  int tot_load, tot_keep;
+  const int b_start = block_excl_scan(load, &tot_load, sm);
+  const int s_start = block_excl_scan(kp, &tot_keep, sm);
+  if (threadIdx.x == 0) s_overflow = (int64_t)tot_keep > cap;
+  __syncthreads();
+  const bool overflow = s_overflow;
+  if (overflow && threadIdx.x == 0) set_status(status, LRM_ERR_CAPACITY);
+  if (e < E) {
+    bucket_start[e] = b_start;
+    keep[e] = overflow ? 0 : kp;
+    seg_offsets[e] = overflow ? 0 : s_start;
+  }
+  if (threadIdx.x == 0) {
+    bucket_start[E] = tot_load;
+    seg_offsets[E] = overflow ? 0 : tot_keep;
+  }
+}
+
+__global__ void __launch_bounds__(256) sel_bucket_kernel(const int32_t* __restrict__ idx,
+                                                         const float* __restrict__ scores, int64_t P, int E,
+                                                         int64_t n_chunks, const int32_t* __restrict__ counts,
+                                                         const int32_t* __restrict__ bucket_start,
+                                                         int32_t* __restrict__ sorted_u,
+                                                         uint32_t* __restrict__ sorted_key,
+                                                         int32_t* __restrict__ row_of_pair) {
+  extern __shared__ int run_all[];  // [kSelWarpsPerBlock][E]
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t c = (int64_t)blockIdx.x * kSelWarpsPerBlock + warp;
+  if (c >= n_chunks) return;
+  int* run = run_all + warp * E;
+  for (int e = lane; e < E; e += 32) run[e] = bucket_start[e] + counts[c * E + e];
+  __syncwarp();
+  const unsigned lt = (1u << lane) - 1u;
+  const int64_t u0 = c * kSelChunk, u1 = min(P, u0 + kSelChunk);
+  for (int64_t base = u0; base < u1; base += 32) {
+    const int64_t u = base + lane;
+    const bool valid = u < u1;
+    int e = valid ? idx[u] : -1;
+    const bool good = valid && e >= 0 && e < E;
+    const uint32_t key = good ? __float_as_uint(scores[u]) : 0u;
+    if (valid && !good) row_of_pair[u] = -1;
+    const int grp = good ? e : -1;
+    const unsigned peers = __match_any_sync(0xffffffffu, grp);
+    int rank = 0;
+    if (good) {
+      rank = __popc(peers & lt);
+      const int pos = run[e] + rank;
+      sorted_u[pos] = (int32_t)u;
+      sorted_key[pos] = key;
+    }
+    __syncwarp();
+    if (good && rank == 0) run[e] += __popc(peers);
+    __syncwarp();
+  }
+}
+
+constexpr int kExpThreads = 512;
+constexpr int kExpIPT = 8;  // bucket elements per thread per round
+
+__global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
+    const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
+    const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u,
+    const uint32_t* __restrict__ sorted_key, int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair) {
+  __shared__ int sm[33];
+  __shared__ int hist[256];
+  __shared__ uint32_t s_prefix;
+  __shared__ int s_need;
+  const int e = blockIdx.x, tid = threadIdx.x;
+  const int b0 = bucket_start[e];
+  const int load = bucket_start[e + 1] - b0;
+  const int keep = keep_arr[e];
+  const int base = seg_offsets[e];
+  const int32_t* bu = sorted_u + b0;
+  const uint32_t* bk = sorted_key + b0;
+
+  if (keep >= load) {
+    for (int i = tid; i < load; i += kExpThreads) {
+      const int u = bu[i];
+      kept_pair[base + i] = u;
+      row_of_pair[u] = base + i;
+    }
+    return;
+  }
+  if (keep <= 0) {
+    for (int i = tid; i < load; i += kExpThreads) row_of_pair[bu[i]] = -1;
+    return;
+  }
+
+  // MSD radix select: find the key value `thr` of the keep-th largest key, and how many of
+  // the keys equal to thr are kept (`need`, >= 1).
+  uint32_t prefix = 0;
+  int need = keep;
+#pragma unroll 1
+  for (int pass = 0; pass < 4; ++pass) {
+    const int shift = 24 - 8 * pass;
+    const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
+    if (tid < 256) hist[tid] = 0;
+    __syncthreads();
+#pragma unroll 4
+    for (int i = tid; i < load; i += kExpThreads) {
+      const uint32_t key = bk[i];
+      if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    // suffix counts over bins, highest bin first: thread b' handles bin 255 - b'
+    const int bin = 255 - tid;
+    const int cnt = tid < 256 ? hist[bin] : 0;
+    int tot;
+    const int above = block_excl_scan(cnt, &tot, sm);  // keys in bins > bin
+    if (tid < 256 && above < need && above + cnt >= need) {
+      s_prefix = prefix | ((uint32_t)bin << shift);
+      s_need = need - above;
+    }
+    __syncthreads();
+    prefix = s_prefix;
+    need = s_need;
+    __syncthreads();
+  }
+  const uint32_t thr = prefix;
+
+  // Ordered keep pass.
+  int run_eq = 0, run_kept = 0;
+  for (int r0 = 0; r0 < load; r0 += kExpThreads * kExpIPT) {
+    const int i0 = r0 + tid * kExpIPT;
+    uint32_t keys[kExpIPT];
+    int n_eq = 0;
+#pragma unroll
+    for (int q = 0; q < kExpIPT; ++q) {
+      const int i = i0 + q;
+      keys[q] = i < load ? bk[i] : 0u;
+      n_eq += (i < load && keys[q] == thr);
+    }
+    int tot_eq;
+    int eq_rank = run_eq + block_excl_scan(n_eq, &tot_eq, sm);
+    bool kf[kExpIPT];
+    int n_kept = 0;
+#pragma unroll
+    for (int q = 0; q < kExpIPT; ++q) {
+      const int i = i0 + q;
+      const bool in = i < load;
+      const bool is_eq = in && keys[q] == thr;
+      kf[q] = in && (keys[q] > thr || (is_eq && eq_rank < need));
+      eq_rank += is_eq;
+      n_kept += kf[q];
+    }
+    int tot_kept;
+    int pos = run_kept + block_excl_scan(n_kept, &tot_kept, sm);
+#pragma unroll
+    for (int q = 0; q < kExpIPT; ++q) {
+      const int i = i0 + q;
+      if (i < load) {
+        const int u = bu[i];
+        if (kf[q]) {
+          kept_pair[base + pos] = u;
+          row_of_pair[u] = base + pos;
+          ++pos;
+        } else {
+          row_of_pair[u] = -1;
+        }
+      }
+    }
+    run_eq += tot_eq;
+    run_kept += tot_kept;
+  }
+}
+
+}  // namespace
+
+void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t P, int32_t E,
+                   int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair, const SelectWs& ws,
+                   int32_t* status, cudaStream_t s) {
+  const int64_t nc = ws.n_chunks;
+  const unsigned cblocks = (unsigned)((nc + kSelWarpsPerBlock - 1) / kSelWarpsPerBlock);
+  const size_t smem = (size_t)kSelWarpsPerBlock * E * sizeof(int);
+  if (nc > 0) sel_count_kernel<<<cblocks, 32 * kSelWarpsPerBlock, smem, s>>>(topk_idx, P, E, nc, ws.counts, status);
+  sel_scan_kernel<<<1, 1024, 0, s>>>(ws.counts, nc, E, quotas, cap, ws.bucket_start, ws.keep, seg_offsets, status);
+  if (nc > 0)
+    sel_bucket_kernel<<<cblocks, 32 * kSelWarpsPerBlock, smem, s>>>(topk_idx, scores, P, E, nc, ws.counts,
+                                                                     ws.bucket_start, ws.sorted_u, ws.sorted_key,
+                                                                     row_of_pair);
+  if (P > 0)
+    sel_expert_kernel<<<E, kExpThreads, 0, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u, ws.sorted_key,
+                                               kept_pair, row_of_pair);
+}
+
+}  // namespace lrm

@@ -1,0 +1,68 @@
+"""CPU checks of the C ABI: the library loads, exports every entry point include/lrm.h declares,
+and rejects bad arguments on the host before any GPU work (no compute call needs a GPU)."""
+import ctypes as C
+import os
+import re
+
+import pytest
+
+from helpers import ensure_built
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_functions():
+    text = open(os.path.join(ROOT, "include", "lrm.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(lrm_[a-z_]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_symbol():
+    lib = ensure_built()
+    names = declared_functions()
+    assert len(names) >= 8
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings():
+    lib = ensure_built()
+    for code in range(0, 11):
+        assert lib.lrm_status_string(code)
+    assert lib.lrm_status_string(99) == b"unknown status"
+
+
+def test_workspace_size_and_host_validation():
+    lib = ensure_built()
+    out = C.c_size_t(0)
+    assert lib.lrm_workspace_size(8192, 8, 128, 2048, 768, 0, C.byref(out)) == 0
+    assert out.value >= 8192 * 8 * 8
+    assert lib.lrm_workspace_size(8, 8, 128, 2048, 768, 0, None) == 1        # null out pointer
+    assert lib.lrm_workspace_size(8, 0, 128, 2048, 768, 0, C.byref(out)) == 1  # k = 0
+    assert lib.lrm_workspace_size(8, 8, 2000, 2048, 768, 0, C.byref(out)) == 2  # E too large
+    assert lib.lrm_workspace_size(8, 8, 128, 2047, 768, 0, C.byref(out)) == 2  # H not a multiple of 8
+    assert lib.lrm_workspace_size(8, 8, 128, 2048, 768, 7, C.byref(out)) == 3  # bad dtype
+    # null device pointers are refused before any launch
+    assert lib.lrm_score(None, None, None, 16, 2, 64, 32, 0, None, None, None) == 1
+    assert lib.lrm_select(None, None, None, 16, 2, 4, 32, None, None, None, None, 0, None, None) == 1
+    assert lib.lrm_compact(None, None, None, None, None, None, 16, 2, 64, 32, 0, 32, None, None, None, None,
+                           None) == 1
+    assert lib.lrm_scatter_dx(None, None, 16, 2, 64, 0, None, None) == 1
+    assert lib.lrm_plan_quotas(None, 16, 2, 4, 0, 8, 10, 0, None, None, None, None, None) == 1
+    # unknown GEMM flag
+    fake = C.c_void_p(0x1000)
+    assert lib.lrm_grouped_backward(fake, fake, fake, fake, fake, fake, fake, 4, 64, 32, 0, 16, fake, fake, fake,
+                                    fake, fake, 1 << 20, 5, None, None) == 1
+    # workspace too small for select
+    assert lib.lrm_select(fake, fake, fake, 16, 2, 4, 32, fake, fake, fake, fake, 8, None, None) == 4
+    # misaligned pointer
+    odd = C.c_void_p(0x1001)
+    assert lib.lrm_score(fake, odd, fake, 16, 2, 64, 32, 0, fake, None, None) == 1
+
+
+def test_python_binding_refuses_cpu_tensors():
+    import torch
+    import pruned_expert_backward_gb300 as lrm
+    ensure_built()
+    with pytest.raises(ValueError):
+        lrm.lrm_score(torch.zeros(4, 2), torch.zeros(4, 8), torch.zeros(4, 2, 8))

@@ -54,7 +54,7 @@ WORKLOADS = {
     # tiny fp32 layer the oracle finishes in well under a second
     "tiny_f32": Workload("tiny_f32", 512, 256, 128, 8, 2, "f32", 1.0, 1.0, ("ratio", 8, 10)),
     # the articles' load example: loads [4, 2, 3] cut to quotas [3, 1, 2]
-    "load_example": Workload("load_example", 9, 8, 4, 3, 1, "f32", 0.0, 1.0, ("explicit", (3, 1, 2)),
+    "load_example": Workload("load_example", 9, 16, 8, 3, 1, "f32", 0.0, 1.0, ("explicit", (3, 1, 2)),
                              topk_idx=(0, 1, 2, 0, 2, 0, 1, 2, 0)),
     # Qwen3-30B-A3B-shaped layer, one 8192-token sequence, drop 20%
     "qwen3_t8k_d20": Workload("qwen3_t8k_d20", 8192, 2048, 768, 128, 8, "bf16", 1.0, 1e-3, ("ratio", 8, 10)),
