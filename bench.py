@@ -184,7 +184,7 @@ def cpu_threads():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--workload", default="qwen3_t8k_d20", choices=sorted(W.WORKLOADS))
@@ -360,7 +360,7 @@ def main():
 def pb_launches(wl, flags):
     """Kernels this library launches per step (memsets excluded)."""
     sel = 4 if wl.P > 0 else 1
-    grouped = 4 if flags else 2
+    grouped = 4 if flags else 5  # SIMT: 4 GEMMs; tcgen05: tile-plan kernel + 4 GEMMs
     return 1 + sel + 1 + grouped + 1
 
 
