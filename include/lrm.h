@@ -178,6 +178,30 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
 lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,
                           lrm_dtype dt, void* dx, cudaStream_t stream);
 
+/*
+ * lrm_select_static — lrm_select for callers that cannot allocate device memory.
+ * The LRMoE pages have no counterpart: this is a deployment convenience of this library.
+ *
+ * Some callers cannot give the library a workspace: a plugin inside a host framework that owns
+ * every device buffer and passes its plugins only their inputs and outputs, or a process whose
+ * device memory is reserved up front by a pool allocator, where a cudaMalloc would fail or break
+ * the pool's accounting.  This entry point takes the same arguments as lrm_select minus ws and
+ * ws_bytes, gives the same results, and allocates nothing: its scratch is a fixed array inside the
+ * library (about 5 MB on every GPU that loads it, held until the process exits).
+ *   - Limit: T*k <= LRM_SELECT_STATIC_MAX_PAIRS (and the usual E, k limits); larger problems
+ *     return LRM_ERR_SHAPE before any GPU work — use lrm_select with a workspace for them.
+ *   - The first call on a device, with that device current, looks up the array's device address
+ *     (cudaGetSymbolAddress) and remembers it; make that first call before any stream capture.
+ *     A failed look-up returns LRM_ERR_CUDA.
+ *   - All calls share the one array and leave their data in it.  Nothing in it needs to start
+ *     at zero, but calls that overlap on the GPU (different streams, or threads without ordering
+ *     between their streams) race on it: serialise them.
+ */
+#define LRM_SELECT_STATIC_MAX_PAIRS 524288
+lrm_status lrm_select_static(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t T,
+                             int32_t k, int32_t E, int64_t cap, int32_t* seg_offsets, int32_t* kept_pair,
+                             int32_t* row_of_pair, int32_t* dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
