@@ -137,14 +137,15 @@ def compact(kept_pair, alpha, g, x, h, phi, k):
     numbers, only without the saving)."""
     kp = np.asarray(kept_pair, dtype=np.int64)
     t = kp // k
-    a = np.asarray(alpha, dtype=np.float64).reshape(-1)[kp]
-    gg = np.asarray(g, dtype=np.float64)[t]
+    # gather the rows first, then widen (same values; avoids widening whole tensors)
+    a = np.asarray(alpha).reshape(-1)[kp].astype(np.float64)
+    gg = np.asarray(g)[t].astype(np.float64)
     dY_c = a[:, None] * gg
-    X_c = np.asarray(x, dtype=np.float64)[t]
-    hh = np.asarray(h, dtype=np.float64)
-    H_c = hh.reshape(-1, hh.shape[-1])[kp]
-    pp = np.asarray(phi, dtype=np.float64)
-    Phi_c = pp.reshape(-1, pp.shape[-1])[kp]
+    X_c = np.asarray(x)[t].astype(np.float64)
+    hh = np.asarray(h)
+    H_c = hh.reshape(-1, hh.shape[-1])[kp].astype(np.float64)
+    pp = np.asarray(phi)
+    Phi_c = pp.reshape(-1, pp.shape[-1])[kp].astype(np.float64)
     return dY_c, X_c, H_c, Phi_c
 
 
