@@ -187,7 +187,7 @@ lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t 
  * device memory is reserved up front by a pool allocator, where a cudaMalloc would fail or break
  * the pool's accounting.  This entry point takes the same arguments as lrm_select minus ws and
  * ws_bytes, gives the same results, and allocates nothing: its scratch is a fixed array inside the
- * library (about 5 MB on every GPU that loads it, held until the process exits).
+ * library (about 12 MB on every GPU that loads it, held until the process exits).
  *   - Limit: T*k <= LRM_SELECT_STATIC_MAX_PAIRS (and the usual E, k limits); larger problems
  *     return LRM_ERR_SHAPE before any GPU work — use lrm_select with a workspace for them.
  *   - The first call on a device, with that device current, looks up the array's device address

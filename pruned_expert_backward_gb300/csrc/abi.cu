@@ -31,6 +31,8 @@ lrm_status after_launch() {
 
 }  // namespace
 
+size_t gemm_ws_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 1)) + 128 * 4 * (size_t)E; }
+
 WsLayout workspace_layout(int64_t P, int32_t E) {
   WsLayout w{};
   const int64_t nc = (P + kSelChunk - 1) / kSelChunk;
@@ -38,9 +40,10 @@ WsLayout workspace_layout(int64_t P, int32_t E) {
   w.counts = off;       off += up(sizeof(int32_t) * (size_t)(nc > 0 ? nc : 1) * E);
   w.bucket_start = off; off += up(sizeof(int32_t) * (size_t)(E + 1));
   w.keep = off;         off += up(sizeof(int32_t) * (size_t)E);
+  w.loads = off;        off += up(sizeof(int32_t) * (size_t)E);
   w.sorted_u = off;     off += up(sizeof(int32_t) * (size_t)(P > 0 ? P : 1));
   w.sorted_key = off;   off += up(sizeof(uint32_t) * (size_t)(P > 0 ? P : 1));
-  w.gemm = off;         off += up(4096);
+  w.gemm = off;         off += up(gemm_ws_bytes(E));
   w.total = off;
   return w;
 }
@@ -124,6 +127,7 @@ lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_
   sw.counts = reinterpret_cast<int32_t*>(b + w.counts);
   sw.bucket_start = reinterpret_cast<int32_t*>(b + w.bucket_start);
   sw.keep = reinterpret_cast<int32_t*>(b + w.keep);
+  sw.loads = reinterpret_cast<int32_t*>(b + w.loads);
   sw.sorted_u = reinterpret_cast<int32_t*>(b + w.sorted_u);
   sw.sorted_key = reinterpret_cast<uint32_t*>(b + w.sorted_key);
   sw.n_chunks = (P + kSelChunk - 1) / kSelChunk;
@@ -166,11 +170,11 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
   GroupedArgs a{seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, E, H, I, cap,
                 dw_gate_up, dw_down, dh_c, dx_c, dev_status};
   if (dt == LRM_BF16 && flags == LRM_GEMM_DEFAULT) {
-    // workspace: the tensor-core path keeps its tile tables (2E+1 ints) at the start
-    if (ws_bytes < up(sizeof(int32_t) * (2 * (size_t)E + 1))) return LRM_ERR_WORKSPACE;
+    // workspace: tile tables and per-expert tensor maps at the start of ws
+    if (ws_bytes < gemm_ws_bytes(E)) return LRM_ERR_WORKSPACE;
     GemmWs gw;
-    gw.tile_counter = static_cast<int32_t*>(ws);
-    gw.tmaps = nullptr;
+    gw.plan = static_cast<int32_t*>(ws);
+    gw.maps = static_cast<char*>(ws) + up(sizeof(int32_t) * (2 * (size_t)E + 1));
     return launch_grouped_tc(a, gw, stream);
   }
   launch_grouped_simt(a, dt, stream);

@@ -11,8 +11,9 @@
 // scaled by alpha_u) into each kept pair's row; the token's k rows of h and phi are one
 // contiguous span, read only where the pair is kept.  16-byte coalesced loads and stores.
 //
-// scatter_dx: one CTA per token; each thread owns one 16-byte column slice, issues the k
-// row loads together and adds them in j order in fp32 (deterministic, no atomics).
+// scatter_dx: a CTA covers several tokens (up to 1024 threads); each thread owns one 16-byte
+// column slice of one token, issues the k row loads together and adds them in j order in
+// fp32 (deterministic, no atomics).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -84,28 +85,34 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
 }
 
 template <typename T>
-__global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
-                                                         const T* __restrict__ dx_c, int k, int H,
-                                                         T* __restrict__ dx) {
+__global__ void __launch_bounds__(1024) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
+                                                          const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
+                                                          int tok_per_blk, T* __restrict__ dx) {
   constexpr int VN = VecTraits<T>::N;
-  __shared__ int64_t s_row[LRM_MAX_TOPK];
-  const int64_t t = blockIdx.x;
-  const int tid = threadIdx.x;
-  if (tid < k) s_row[tid] = row_of_pair[t * k + tid];
+  extern __shared__ int64_t s_rows[];  // [tok_per_blk][k]
+  const int64_t t0 = (int64_t)blockIdx.x * tok_per_blk;
+  for (int i = threadIdx.x; i < tok_per_blk * k; i += blockDim.x) {
+    const int64_t u = t0 * k + i;
+    s_rows[i] = u < n_tok * k ? (int64_t)row_of_pair[u] : -1;
+  }
   __syncthreads();
   const int nvH = H / VN;
-  for (int v = tid; v < nvH; v += blockDim.x) {
+  for (int w = threadIdx.x; w < tok_per_blk * nvH; w += blockDim.x) {
+    const int tt = w / nvH, v = w - tt * nvH;
+    const int64_t t = t0 + tt;
+    if (t >= n_tok) break;
+    const int64_t* rows = s_rows + tt * k;
     uint4 vals[LRM_MAX_TOPK];
 #pragma unroll
     for (int j = 0; j < LRM_MAX_TOPK; ++j) {
-      if (j < k && s_row[j] >= 0) vals[j] = ld_stream16(dx_c + s_row[j] * H + v * VN);
+      if (j < k && rows[j] >= 0) vals[j] = ld_stream16(dx_c + rows[j] * H + v * VN);
     }
     float acc[VN];
 #pragma unroll
     for (int q = 0; q < VN; ++q) acc[q] = 0.f;
 #pragma unroll
     for (int j = 0; j < LRM_MAX_TOPK; ++j) {
-      if (j < k && s_row[j] >= 0) {
+      if (j < k && rows[j] >= 0) {
         float f[VN];
         unpack(vals[j], f);
 #pragma unroll
@@ -117,7 +124,7 @@ __global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restri
 }
 
 int threads_for(int n_vec) {
-  int t = n_vec < 256 ? n_vec : 256;
+  int t = n_vec < 1024 ? n_vec : 1024;
   t = (t + 31) / 32 * 32;
   return t < 32 ? 32 : t;
 }
@@ -143,12 +150,18 @@ void launch_compact(const int32_t* row_of_pair, const float* alpha, const void* 
 void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H, lrm_dtype dt,
                        void* dx, cudaStream_t s) {
   if (T == 0) return;
+  const int nvH = H / (dt == LRM_BF16 ? 8 : 4);
+  int tok = nvH >= 1024 ? 1 : 1024 / nvH;  // one thread per 16-byte column slice, up to 1024 threads
+  if (tok > 64) tok = 64;
+  const int threads = threads_for(nvH * tok);
+  const unsigned blocks = (unsigned)((T + tok - 1) / tok);
+  const size_t smem = sizeof(int64_t) * tok * k;
   if (dt == LRM_BF16) {
     using B = __nv_bfloat16;
-    scatter_dx_kernel<B><<<(unsigned)T, threads_for(H / 8), 0, s>>>(row_of_pair, (const B*)dx_c, k, H, (B*)dx);
+    scatter_dx_kernel<B><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok, (B*)dx);
   } else {
-    scatter_dx_kernel<float><<<(unsigned)T, threads_for(H / 4), 0, s>>>(row_of_pair, (const float*)dx_c, k, H,
-                                                                        (float*)dx);
+    scatter_dx_kernel<float><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H, tok,
+                                                           (float*)dx);
   }
 }
 

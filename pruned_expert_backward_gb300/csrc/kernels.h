@@ -11,25 +11,29 @@
 namespace lrm {
 
 // Selection works on warp-sized chunks of this many consecutive pairs.
-constexpr int kSelChunk = 2048;
+constexpr int kSelChunk = 256;
 constexpr int kSelWarpsPerBlock = 8;
 
 struct SelectWs {
   int32_t* counts;        // [n_chunks][E]  per-chunk expert counts, then exclusive bases
   int32_t* bucket_start;  // [E+1]          start of each expert's bucket in sorted_u
   int32_t* keep;          // [E]            min(max(quota,0), load), or 0 on capacity overflow
+  int32_t* loads;         // [E]            pairs routed to each expert
   int32_t* sorted_u;      // [P]            pairs grouped by expert, u ascending
   uint32_t* sorted_key;   // [P]            score bits in the same order
   int64_t n_chunks;
 };
 
+// Scratch of the tensor-core grouped GEMMs: tile tables, then 4*E per-expert TMA tensor maps
+// (128 bytes each, 128-byte aligned) built on the device from seg_offsets.
 struct GemmWs {
-  int32_t* tile_counter;  // [4] dynamic tile queues (zeroed by the launcher)
-  void* tmaps;            // reserved
+  int32_t* plan;  // [2E+1]
+  void* maps;     // [4][E] CUtensorMap
 };
+size_t gemm_ws_bytes(int32_t E);
 
 struct WsLayout {
-  size_t counts, bucket_start, keep, sorted_u, sorted_key, gemm, total;
+  size_t counts, bucket_start, keep, loads, sorted_u, sorted_key, gemm, total;
 };
 WsLayout workspace_layout(int64_t P, int32_t E);
 

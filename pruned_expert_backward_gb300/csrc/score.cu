@@ -5,21 +5,22 @@
 // the down projection's weight gradient, so ||G_u||_F^2 = alpha_u^2 * ||g_t||^2 * ||phi_u||^2
 // and no gradient matrix has to be formed.
 //
-// One group of k warps per token.  The token's g_t row is split over all k warps (each row
-// of g is read once), warp j reduces phi_u for u = t*k + j; the k phi rows of a token are
-// contiguous, so a block streams one contiguous span of memory.  All loads are 16-byte,
-// coalesced, marked evict-first (nothing here is re-read).  HBM-bound.
+// One group of k warps per token, several tokens per CTA (up to 1024 threads).  The token's
+// g_t row is split over its k warps (each row of g is read once), warp j reduces phi_u for
+// u = t*k + j; the k phi rows of consecutive tokens are contiguous, so a CTA streams one
+// contiguous span of memory.  All loads are 16-byte, coalesced, not allocated in L1 (nothing
+// here is re-read).  HBM-bound.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace lrm {
 
 template <typename T>
-__global__ void __launch_bounds__(512) score_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
+__global__ void __launch_bounds__(1024) score_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
                                                     const T* __restrict__ phi, int64_t n_tok, int k, int H, int I,
                                                     float* __restrict__ scores, int32_t* status) {
   constexpr int VN = VecTraits<T>::N;
-  __shared__ float g_part[16];
+  __shared__ float g_part[32];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int tok_per_blk = blockDim.x / (32 * k);
   const int tok_in_blk = warp / k, j = warp - tok_in_blk * k;
@@ -62,7 +63,7 @@ __global__ void __launch_bounds__(512) score_kernel(const float* __restrict__ al
 void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
                   lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s) {
   if (T == 0) return;
-  const int tok_per_blk = k >= 8 ? 1 : 8 / k;
+  const int tok_per_blk = k >= 32 ? 1 : 32 / k;  // up to 32 warps: several tokens per CTA
   const int threads = 32 * k * tok_per_blk;
   const int64_t blocks = (T + tok_per_blk - 1) / tok_per_blk;
   if (dt == LRM_BF16)

@@ -6,10 +6,12 @@
 //
 // Four launches, all deterministic:
 //  1. count:   each warp owns a chunk of kSelChunk consecutive pairs and counts its experts.
-//  2. scan:    per expert, exclusive scan of the chunk counts (bucket bases), loads, kept
-//              counts min(quota, load) and the segment offsets (capacity checked here).
-//  3. bucket:  stable scatter of the pairs into expert buckets (u ascending) with their
-//              score bits; ranks within a warp come from __match_any_sync.
+//  2. scan:    one CTA per expert: exclusive scan of that expert's chunk counts (bucket
+//              bases inside the expert's bucket) and its load.
+//  3. bucket:  every CTA derives the expert-level prefixes (bucket starts, kept counts
+//              min(quota, load), segment offsets, capacity check; CTA 0 publishes them),
+//              then scatters its chunks' pairs stably into the expert buckets (u ascending)
+//              with their score bits; ranks within a warp come from __match_any_sync.
 //  4. expert:  one CTA per expert: MSD radix select (4 x 8 bits) of the quota-th largest
 //              score in the bucket, then one ordered pass that keeps everything above the
 //              threshold plus the first `need` pairs equal to it, and writes kept_pair and
@@ -74,58 +76,90 @@ __global__ void __launch_bounds__(256) sel_count_kernel(const int32_t* __restric
   for (int e = lane; e < E; e += 32) counts[c * E + e] = h[e];
 }
 
-__global__ void __launch_bounds__(1024) sel_scan_kernel(int32_t* __restrict__ counts, int64_t n_chunks, int E,
-                                                        const int32_t* __restrict__ quotas, int64_t cap,
-                                                        int32_t* __restrict__ bucket_start, int32_t* __restrict__ keep,
-                                                        int32_t* __restrict__ seg_offsets, int32_t* status) {
+// One CTA per expert: exclusive scan down the expert's column of chunk counts.
+__global__ void __launch_bounds__(1024) sel_colscan_kernel(int32_t* __restrict__ counts, int64_t n_chunks, int E,
+                                                           int32_t* __restrict__ loads) {
   __shared__ int sm[33];
-  __shared__ int s_overflow;
-  const int e = threadIdx.x;  // E <= 1024 = blockDim.x
-  int load = 0;
-  if (e < E) {
-#pragma unroll 8
-    for (int64_t c = 0; c < n_chunks; ++c) {
-      const int v = counts[c * E + e];
-      counts[c * E + e] = load;
-      load += v;
-    }
-  }
-  int kp = 0;
-  if (e < E) {
-    const int q = quotas[e];
-    kp = q < 0 ? 0 : (q > load ? load : q);
-  }
-  int tot_load, tot_keep;
-  const int b_start = block_excl_scan(load, &tot_load, sm);
-  const int s_start = block_excl_scan(kp, &tot_keep, sm);
-  if (threadIdx.x == 0) s_overflow = (int64_t)tot_keep > cap;
+  __shared__ int s_run;
+  const int e = blockIdx.x;
+  if (threadIdx.x == 0) s_run = 0;
   __syncthreads();
-  const bool overflow = s_overflow;
-  if (overflow && threadIdx.x == 0) set_status(status, LRM_ERR_CAPACITY);
-  if (e < E) {
-    bucket_start[e] = b_start;
-    keep[e] = overflow ? 0 : kp;
-    seg_offsets[e] = overflow ? 0 : s_start;
+  for (int64_t c0 = 0; c0 < n_chunks; c0 += blockDim.x) {
+    const int64_t c = c0 + threadIdx.x;
+    const int v = c < n_chunks ? counts[c * E + e] : 0;
+    int tot;
+    const int ex = block_excl_scan(v, &tot, sm);
+    if (c < n_chunks) counts[c * E + e] = s_run + ex;
+    __syncthreads();
+    if (threadIdx.x == 0) s_run += tot;
+    __syncthreads();
   }
-  if (threadIdx.x == 0) {
-    bucket_start[E] = tot_load;
-    seg_offsets[E] = overflow ? 0 : tot_keep;
-  }
+  if (threadIdx.x == 0) loads[e] = s_run;
 }
 
-__global__ void __launch_bounds__(256) sel_bucket_kernel(const int32_t* __restrict__ idx,
-                                                         const float* __restrict__ scores, int64_t P, int E,
-                                                         int64_t n_chunks, const int32_t* __restrict__ counts,
-                                                         const int32_t* __restrict__ bucket_start,
-                                                         int32_t* __restrict__ sorted_u,
-                                                         uint32_t* __restrict__ sorted_key,
-                                                         int32_t* __restrict__ row_of_pair) {
-  extern __shared__ int run_all[];  // [kSelWarpsPerBlock][E]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+__global__ void __launch_bounds__(256) sel_bucket_kernel(
+    const int32_t* __restrict__ idx, const float* __restrict__ scores, int64_t P, int E, int64_t n_chunks,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ loads, const int32_t* __restrict__ quotas,
+    int64_t cap, int32_t* __restrict__ bucket_start, int32_t* __restrict__ keep, int32_t* __restrict__ seg_offsets,
+    int32_t* __restrict__ sorted_u, uint32_t* __restrict__ sorted_key, int32_t* __restrict__ row_of_pair,
+    int32_t* status) {
+  extern __shared__ int sh[];
+  int* s_bstart = sh;                       // [E]
+  int* run_all = sh + E;                    // [kSelWarpsPerBlock][E]
+  __shared__ int sm[33];
+  __shared__ int s_base_l, s_base_k, s_overflow;
+  const int tid = threadIdx.x;
+
+  // expert-level prefixes (E <= 1024: at most 4 experts per thread, processed in order)
+  if (tid == 0) { s_base_l = 0; s_base_k = 0; }
+  __syncthreads();
+  int kp_mine[4];
+  for (int r = 0; r < (E + 255) / 256; ++r) {
+    const int e = r * 256 + tid;
+    const int l = e < E ? loads[e] : 0;
+    int kp = 0;
+    if (e < E) {
+      const int q = quotas[e];
+      kp = q < 0 ? 0 : (q > l ? l : q);
+    }
+    kp_mine[r] = kp;
+    int tl, tk;
+    const int xl = block_excl_scan(l, &tl, sm);
+    const int xk = block_excl_scan(kp, &tk, sm);
+    if (e < E) {
+      s_bstart[e] = s_base_l + xl;
+      run_all[e] = s_base_k + xk;  // temporarily: segment start
+    }
+    __syncthreads();
+    if (tid == 0) { s_base_l += tl; s_base_k += tk; }
+    __syncthreads();
+  }
+  if (tid == 0) s_overflow = (int64_t)s_base_k > cap;
+  __syncthreads();
+  const bool overflow = s_overflow;
+  if (blockIdx.x == 0) {
+    for (int r = 0; r < (E + 255) / 256; ++r) {
+      const int e = r * 256 + tid;
+      if (e < E) {
+        bucket_start[e] = s_bstart[e];
+        keep[e] = overflow ? 0 : kp_mine[r];
+        seg_offsets[e] = overflow ? 0 : run_all[e];
+      }
+    }
+    if (tid == 0) {
+      bucket_start[E] = s_base_l;
+      seg_offsets[E] = overflow ? 0 : s_base_k;
+      if (overflow) set_status(status, LRM_ERR_CAPACITY);
+    }
+  }
+  __syncthreads();
+
+  // stable scatter of this block's chunks
+  const int warp = tid >> 5, lane = tid & 31;
   const int64_t c = (int64_t)blockIdx.x * kSelWarpsPerBlock + warp;
   if (c >= n_chunks) return;
   int* run = run_all + warp * E;
-  for (int e = lane; e < E; e += 32) run[e] = bucket_start[e] + counts[c * E + e];
+  for (int e = lane; e < E; e += 32) run[e] = s_bstart[e] + counts[c * E + e];
   __syncwarp();
   const unsigned lt = (1u << lane) - 1u;
   const int64_t u0 = c * kSelChunk, u1 = min(P, u0 + kSelChunk);
@@ -270,11 +304,10 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
   const unsigned cblocks = (unsigned)((nc + kSelWarpsPerBlock - 1) / kSelWarpsPerBlock);
   const size_t smem = (size_t)kSelWarpsPerBlock * E * sizeof(int);
   if (nc > 0) sel_count_kernel<<<cblocks, 32 * kSelWarpsPerBlock, smem, s>>>(topk_idx, P, E, nc, ws.counts, status);
-  sel_scan_kernel<<<1, 1024, 0, s>>>(ws.counts, nc, E, quotas, cap, ws.bucket_start, ws.keep, seg_offsets, status);
-  if (nc > 0)
-    sel_bucket_kernel<<<cblocks, 32 * kSelWarpsPerBlock, smem, s>>>(topk_idx, scores, P, E, nc, ws.counts,
-                                                                     ws.bucket_start, ws.sorted_u, ws.sorted_key,
-                                                                     row_of_pair);
+  sel_colscan_kernel<<<E, 1024, 0, s>>>(ws.counts, nc, E, ws.loads);
+  sel_bucket_kernel<<<cblocks > 0 ? cblocks : 1, 32 * kSelWarpsPerBlock, smem + E * sizeof(int), s>>>(
+      topk_idx, scores, P, E, nc, ws.counts, ws.loads, quotas, cap, ws.bucket_start, ws.keep, seg_offsets,
+      ws.sorted_u, ws.sorted_key, row_of_pair, status);
   if (P > 0)
     sel_expert_kernel<<<E, kExpThreads, 0, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u, ws.sorted_key,
                                                kept_pair, row_of_pair);

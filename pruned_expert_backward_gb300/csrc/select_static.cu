@@ -5,7 +5,7 @@
 // outputs, or a process whose device memory is reserved up front by a pool allocator, where
 // a cudaMalloc would fail or break the pool's accounting.  For them this entry point runs
 // the same four selection kernels as lrm_select, with their scratch in a fixed array that
-// is part of the library image on every GPU that loads it (about 5 MB, held until exit).
+// is part of the library image on every GPU that loads it (about 12 MB, held until exit).
 //
 // Set-up: the first call on a device (with that device current) looks up the array's
 // device address with cudaGetSymbolAddress and keeps it; later calls on that device reuse
@@ -25,11 +25,12 @@ namespace {
 constexpr int64_t kStaticMaxPairs = LRM_SELECT_STATIC_MAX_PAIRS;
 
 constexpr size_t round256(size_t v) { return (v + 255) / 256 * 256; }
-// Same regions as workspace_layout(kStaticMaxPairs, LRM_MAX_EXPERTS), sized at compile time.
+// The selection regions of workspace_layout(kStaticMaxPairs, LRM_MAX_EXPERTS), sized at compile time
+// (the grouped-GEMM region that follows them in a workspace is not needed here).
 constexpr size_t kStaticBytes =
     round256(sizeof(int32_t) * (size_t)((kStaticMaxPairs + kSelChunk - 1) / kSelChunk) * LRM_MAX_EXPERTS) +
-    round256(sizeof(int32_t) * (LRM_MAX_EXPERTS + 1)) + round256(sizeof(int32_t) * LRM_MAX_EXPERTS) +
-    round256(sizeof(int32_t) * kStaticMaxPairs) + round256(sizeof(uint32_t) * kStaticMaxPairs) + round256(4096);
+    round256(sizeof(int32_t) * (LRM_MAX_EXPERTS + 1)) + 2 * round256(sizeof(int32_t) * LRM_MAX_EXPERTS) +
+    round256(sizeof(int32_t) * kStaticMaxPairs) + round256(sizeof(uint32_t) * kStaticMaxPairs);
 
 static __device__ __align__(256) unsigned char g_select_scratch[kStaticBytes];
 
@@ -69,13 +70,14 @@ extern "C" lrm_status lrm_select_static(const int32_t* topk_idx, const float* sc
   if (P > 0 && (!topk_idx || !scores || !row_of_pair)) return LRM_ERR_INVALID_ARG;
   if (cap > 0 && !kept_pair) return LRM_ERR_INVALID_ARG;
   const WsLayout w = workspace_layout(P, E);
-  if (w.total > kStaticBytes) return LRM_ERR_SHAPE;
+  if (w.gemm > kStaticBytes) return LRM_ERR_SHAPE;
   char* b = static_cast<char*>(scratch_for_current_device());
   if (b == nullptr) return LRM_ERR_CUDA;
   SelectWs sw;
   sw.counts = reinterpret_cast<int32_t*>(b + w.counts);
   sw.bucket_start = reinterpret_cast<int32_t*>(b + w.bucket_start);
   sw.keep = reinterpret_cast<int32_t*>(b + w.keep);
+  sw.loads = reinterpret_cast<int32_t*>(b + w.loads);
   sw.sorted_u = reinterpret_cast<int32_t*>(b + w.sorted_u);
   sw.sorted_key = reinterpret_cast<uint32_t*>(b + w.sorted_key);
   sw.n_chunks = (P + kSelChunk - 1) / kSelChunk;
