@@ -14,11 +14,17 @@
 //   VK         dW[e] = A[e]^T B[e] over the segment rows (K = R_e):
 //              dW_down = dy_c^T phi_c, dW_gate_up = dh_c^T x_c; fp32 out
 //
-// CTA layout (320 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues the MMAs
-// (one thread), warps 2-9 drain the accumulators (tcgen05.ld; two warps per 32-row TMEM
-// quarter, each taking half of the columns).  Tiles are 128 x 256 with 64-deep K slices;
-// 4 smem stages of 48 KB; two 256-column fp32 accumulators in TMEM so the epilogue of one
-// tile overlaps the MMAs of the next.
+// CTAs run in pairs (a cluster of two) and use the 2-SM MMA: the leader (even) CTA issues
+// tcgen05.mma.cta_group::2, which computes a 256 x 256 tile from both CTAs' shared memory
+// (each CTA stages its own 128 rows of A and its own 128 columns of B) into both CTAs' TMEM
+// (128 rows each).  Per SM that is 32 KB of operands per 64-deep K slice instead of 48 KB
+// for a 128 x 256 single-SM tile, and 6 stages fit in shared memory.
+// CTA layout (320 threads): warp 0 issues TMA loads (both CTAs; they complete on the
+// leader's full barrier), warp 1 owns TMEM (allocated collectively by the pair) and, in the
+// leader, issues the MMAs from one thread; warps 2-9 drain this CTA's accumulator rows
+// (tcgen05.ld; two warps per 32-row TMEM quarter, each taking half of the columns).  Two
+// 256-column fp32 accumulators in TMEM let the epilogue of one tile overlap the MMAs of the
+// next; both CTAs' epilogues release an accumulator on the leader's barrier.
 //
 // Shared-memory operand layouts are the 128-byte-swizzled canonical forms:
 //   K-major  (rows of 64 K-elements = 128 B): SBO = 1024 B between 8-row groups;
@@ -41,13 +47,13 @@ namespace lrm {
 
 namespace {
 
-constexpr int kBM = 128, kBN = 256, kBK = 64;
-constexpr int kMaxStages = 4;
-constexpr int kVmStages = 4;
-constexpr int kVkStages = 4;
-constexpr int kABytes = kBM * kBK * 2;  // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;  // 32 KB
-constexpr int kStageBytes = kABytes + kBBytes;
+constexpr int kBM = 128;  // output rows per CTA; a CTA pair computes 256-row tiles
+constexpr int kBN = 256;  // output columns of a pair tile; each CTA stages half of B
+constexpr int kBK = 64;
+constexpr int kStages = 6;
+constexpr int kABytes = kBM * kBK * 2;            // 16 KB: this CTA's 128 rows of A
+constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 columns of B
+constexpr int kStageBytes = kABytes + kBHalfBytes;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each taking half of the columns
 constexpr int kThreads = 64 + 32 * kEpiWarps;
 // Epilogue staging per epilogue warp: a 32 x 32 fp32 block with rows padded to 33 floats
@@ -61,7 +67,6 @@ enum Kind { VM_SWIGLU = 0, VM_STORE = 1, VK = 2 };
 
 struct TcParams {
   int kind;
-  int stages;
   int E;
   int M, N, K;         // VM: N, K fixed (M per expert); VK: M, N fixed (K per expert)
   int nM, nN;          // tile counts along the fixed dims (VK: nM and nN; VM: nN)
@@ -120,18 +125,42 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   set_status(status, LRM_ERR_TIMEOUT);
   return false;
 }
-__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t bar) {
+// Cluster helpers.  CTAs run in pairs (a cluster of two); the even CTA is the MMA leader.
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release;" ::: "memory");
+  asm volatile("barrier.cluster.wait.acquire;" ::: "memory");
+}
+// Address, in the cluster shared window, of the same shared offset in CTA `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(uint32_t local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cbar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cluster.b64 _, [%0], %1;" ::"r"(cbar), "r"(bytes) : "memory");
+}
+// TMA load into this CTA's shared memory that completes on an mbarrier of either CTA of the pair.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];"
-      ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(bar)
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cbar)
       : "memory");
 }
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
-      "[%5];" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
       : "memory");
 }
 // A tensor map written by another kernel (generic proxy) must be acquired by the tensormap
@@ -141,12 +170,12 @@ __device__ __forceinline__ void tensormap_acquire(const CUtensorMap* m) {
                : "memory");
 }
 __device__ __forceinline__ void tmem_alloc(uint32_t holder, uint32_t ncols) {
-  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder), "r"(ncols)
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(holder), "r"(ncols)
                : "memory");
-  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() {
   asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -157,12 +186,16 @@ __device__ __forceinline__ void mma_bf16(uint32_t tmem_d, uint64_t adesc, uint64
   asm volatile(
       "{\n\t.reg .pred p;\n\t"
       "setp.ne.b32 p, %4, 0;\n\t"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-__device__ __forceinline__ void mma_commit(uint32_t bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
+// Completion of this CTA pair's MMAs arrives on the mbarrier at the same offset in both CTAs.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(bar),
+      "h"((uint16_t)0x3)
+      : "memory");
 }
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
   asm volatile(
@@ -181,37 +214,43 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint3
   return (uint64_t)((addr >> 4) & 0x3FFFu) | ((uint64_t)((lbo >> 4) & 0x3FFFu) << 16) |
          ((uint64_t)((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
 }
-// Instruction descriptor of kind::f16: D fp32, A and B bf16, dense, M = 128, N = 256.
+// Instruction descriptor of kind::f16: D fp32, A and B bf16, dense, M = 256 (the CTA pair),
+// N = 256.
 __host__ __device__ constexpr uint32_t instr_desc(uint32_t a_mn_major, uint32_t b_mn_major) {
   return (1u << 4) | (1u << 7) | (1u << 10) | (a_mn_major << 15) | (b_mn_major << 16) |
-         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)(kBM >> 4) << 24);
+         ((uint32_t)(kBN >> 3) << 17) | ((uint32_t)((2 * kBM) >> 4) << 24);
 }
 
 // ---------------------------------------------------------------- tile decode --------
+// Work is handed out in pair tiles: a cluster of two CTAs computes two vertically adjacent
+// 128-row tiles (rank 0 the upper, rank 1 the lower) that share the same 256 B columns.
 struct Tile {
   int e;
-  int row0, row_end;  // VM: output rows; VK: reduction rows
-  int m0, n0;         // VK: output tile origin; VM: n0 only
+  int row0, row_end;  // VM: this CTA's output rows; VK: the expert's reduction rows
+  int m0, n0;         // VK: output tile origin of this CTA; VM: n0 only
   int k_iters;
+  bool has_rows;      // this CTA's half of the pair tile holds output rows
 };
 
 // The tile tables (seg_offsets and the plan) are tiny and read through the read-only cache.
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
-  return p.kind == VK ? p.E * p.nM * p.nN : __ldg(p.plan + p.E) * p.nN;
+  return p.kind == VK ? p.E * ((p.nM + 1) / 2) * p.nN : __ldg(p.plan + p.E) * p.nN;
 }
 
-__device__ __forceinline__ Tile decode(const TcParams& p, int t) {
+__device__ __forceinline__ Tile decode(const TcParams& p, int t, int rank) {
   Tile d;
   if (p.kind == VK) {
-    const int per = p.nM * p.nN;
+    const int nMp = (p.nM + 1) / 2;
+    const int per = nMp * p.nN;
     const int ei = t / per, r = t - ei * per;
     d.e = __ldg(p.plan + p.E + 1 + ei);
-    const int mt = r / p.nN, nt = r - mt * p.nN;
-    d.m0 = mt * kBM;
+    const int mp = r / p.nN, nt = r - mp * p.nN;
+    d.m0 = (2 * mp + rank) * kBM;
     d.n0 = nt * kBN;
     d.row0 = __ldg(p.seg + d.e);
     d.row_end = __ldg(p.seg + d.e + 1);
     d.k_iters = (d.row_end - d.row0 + kBK - 1) / kBK;
+    d.has_rows = d.m0 < p.M;
   } else {
     const int mg = t / p.nN, nt = t - mg * p.nN;
     int lo = 0, hi = p.E;  // largest e with prefix[e] <= mg
@@ -220,17 +259,19 @@ __device__ __forceinline__ Tile decode(const TcParams& p, int t) {
       if (__ldg(p.plan + mid) <= mg) lo = mid; else hi = mid;
     }
     d.e = lo;
-    d.row0 = __ldg(p.seg + lo) + (mg - __ldg(p.plan + lo)) * kBM;
-    d.row_end = min(__ldg(p.seg + lo + 1), d.row0 + kBM);
+    const int seg_end = __ldg(p.seg + lo + 1);
+    d.row0 = __ldg(p.seg + lo) + (mg - __ldg(p.plan + lo)) * (2 * kBM) + rank * kBM;
+    d.row_end = min(seg_end, d.row0 + kBM);
     d.m0 = 0;
     d.n0 = nt * kBN;
     d.k_iters = (p.K + kBK - 1) / kBK;
+    d.has_rows = d.row0 < seg_end;
   }
   return d;
 }
 
-__host__ __device__ constexpr uint32_t epi_offset(int stages) { return (uint32_t)stages * kStageBytes; }
-__host__ __device__ constexpr uint32_t bar_offset(int stages) { return epi_offset(stages) + kEpiWarps * kEpiBytes; }
+__host__ __device__ constexpr uint32_t epi_offset() { return (uint32_t)kStages * kStageBytes; }
+__host__ __device__ constexpr uint32_t bar_offset() { return epi_offset() + kEpiWarps * kEpiBytes; }
 
 // ---------------------------------------------------------------- the kernel ---------
 __global__ void __launch_bounds__(kThreads, 1)
@@ -238,47 +279,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int S = p.stages;
-  uint8_t* epi = smem + epi_offset(S);
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_offset(S));
-  // bars: full[kMaxStages], empty[kMaxStages], acc_full[2], acc_empty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * kMaxStages + 5);
+  constexpr int S = kStages;
+  uint8_t* epi = smem + epi_offset();
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_offset());
+  // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + kMaxStages);
-  const uint32_t accf0 = smem_u32(bars + 2 * kMaxStages), acce0 = smem_u32(bars + 2 * kMaxStages + 2);
-  const uint32_t drain = smem_u32(bars + 2 * kMaxStages + 4);
+  const int rank = (int)cluster_rank();
+  const bool leader = rank == 0;
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+  const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
+  const uint32_t accf0 = smem_u32(bars + 2 * S), acce0 = smem_u32(bars + 2 * S + 2);
+  const uint32_t drain = smem_u32(bars + 2 * S + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 1);
-      mbar_init(empty0 + 8 * s, 1);
+      mbar_init(full0 + 8 * s, 2);   // leader's: both producers arrive with their byte counts
+      mbar_init(empty0 + 8 * s, 1);  // the leader's MMA commit, multicast to the pair
     }
     mbar_init(accf0, 1);
     mbar_init(accf0 + 8, 1);
-    mbar_init(acce0, kEpiWarps);
-    mbar_init(acce0 + 8, kEpiWarps);
+    mbar_init(acce0, 2 * kEpiWarps);  // leader's: the epilogue warps of both CTAs
+    mbar_init(acce0 + 8, 2 * kEpiWarps);
     mbar_init(drain, 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);
+  if (warp == 1) tmem_alloc(smem_u32(tmem_holder), kTmemCols);  // collective over the pair
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // both CTAs' barriers exist before any remote operation targets them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
   const int n_tiles = total_tiles(p);
   volatile int* abortv = abort_flag;
+  const uint32_t full_lead = cluster_addr(full0, 0), acce_lead = cluster_addr(acce0, 0);
 
   if (warp == 0) {
     // ------------------------------------------------------------ TMA producer -------
+    // Both CTAs load their own 128 rows of A and their own 128 columns of B; the loads
+    // complete on the leader's full barrier, which the leader's MMA waits on.
     if (lane == 0) {
       uint32_t it = 0;
       bool ok = true;
       int last_e = -1;
-      for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-        const Tile d = decode(p, t);
+      for (int t = pair; t < n_tiles && ok; t += n_pairs) {
+        const Tile d = decode(p, t, rank);
         const CUtensorMap* ma = &tmA;
         const CUtensorMap* mb = &tmB;
         if (p.kind == VK) {
@@ -290,68 +338,72 @@ __global__ void __launch_bounds__(kThreads, 1)
             last_e = d.e;
           }
         }
+        const int nb = d.n0 + rank * (kBN / 2);  // this CTA's half of the B columns
         for (int kb = 0; kb < d.k_iters; ++kb, ++it) {
           const uint32_t s = it % S, ph = (it / S) & 1u;
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abortv, p.status)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(smem + s * kStageBytes), b_dst = a_dst + kABytes;
-          const uint32_t fb = full0 + 8 * s;
-          mbar_expect_tx(fb, kStageBytes);
+          const uint32_t fb = full_lead + 8 * s;
+          mbar_expect_tx_cluster(fb, kBHalfBytes + (d.has_rows ? kABytes : 0));
           if (p.kind == VK) {
             const int r = d.row0 + kb * kBK;
-            tma_load_2d(a_dst, ma, d.m0, r, fb);
-            tma_load_2d(a_dst + 8192, ma, d.m0 + 64, r, fb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + 8192 * j, mb, d.n0 + 64 * j, r, fb);
+            if (d.has_rows) {
+              tma_load_2d_pair(a_dst, ma, d.m0, r, fb);
+              tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r, fb);
+            }
+            tma_load_2d_pair(b_dst, mb, nb, r, fb);
+            tma_load_2d_pair(b_dst + 8192, mb, nb + 64, r, fb);
           } else {
-            tma_load_2d(a_dst, &tmA, kb * kBK, d.row0, fb);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) tma_load_3d(b_dst + 8192 * j, &tmB, d.n0 + 64 * j, kb * kBK, d.e, fb);
+            if (d.has_rows) tma_load_2d_pair(a_dst, &tmA, kb * kBK, d.row0, fb);
+            tma_load_3d_pair(b_dst, &tmB, nb, kb * kBK, d.e, fb);
+            tma_load_3d_pair(b_dst + 8192, &tmB, nb + 64, kb * kBK, d.e, fb);
           }
         }
       }
-      // drain: every load this thread issued must have landed before the CTA exits
+      // drain: every stage this thread filled has been consumed (so its data landed)
       const uint32_t first = it > (uint32_t)S ? it - S : 0u;
-      for (uint32_t i = first; i < it; ++i) mbar_wait(full0 + 8 * (i % S), (i / S) & 1u, abortv, p.status, false);
+      for (uint32_t i = first; i < it; ++i) mbar_wait(empty0 + 8 * (i % S), (i / S) & 1u, abortv, p.status, false);
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer ---------
-    const bool a_mn = p.kind == VK;
-    const uint32_t idesc = instr_desc(a_mn ? 1u : 0u, 1u);
-    uint32_t it = 0;
-    int lt = 0;
-    bool ok = true;
-    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++lt) {
-      const Tile d = decode(p, t);
-      const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
-      if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
-      tc_fence_after();
-      const uint32_t tmem_d = tmem_base + acc * kBN;
-      for (int kb = 0; kb < d.k_iters; ++kb, ++it) {
-        const uint32_t s = it % S, ph = (it / S) & 1u;
-        if (!mbar_wait(full0 + 8 * s, ph, abortv, p.status)) { ok = false; break; }
+    // Only the leader issues: tcgen05.mma.cta_group::2 computes the 256 x 256 pair tile from
+    // both CTAs' shared memory into both CTAs' TMEM (128 rows each).
+    if (leader) {
+      const uint32_t idesc = instr_desc(p.kind == VK ? 1u : 0u, 1u);
+      uint32_t it = 0;
+      int lt = 0;
+      bool ok = true;
+      for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+        const Tile d = decode(p, t, 0);
+        const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
+        if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
         tc_fence_after();
-        uint8_t* a_st = smem + s * kStageBytes;
-        uint8_t* b_st = a_st + kABytes;
-        if (lane == 0) {
-          const uint32_t a_addr = smem_u32(a_st), b_addr = smem_u32(b_st);
+        const uint32_t tmem_d = tmem_base + acc * kBN;
+        for (int kb = 0; kb < d.k_iters; ++kb, ++it) {
+          const uint32_t s = it % S, ph = (it / S) & 1u;
+          if (!mbar_wait(full0 + 8 * s, ph, abortv, p.status)) { ok = false; break; }
+          tc_fence_after();
+          if (lane == 0) {
+            const uint32_t a_addr = smem_u32(smem + s * kStageBytes), b_addr = a_addr + kABytes;
 #pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk) {
-            const uint64_t adesc = a_mn ? smem_desc(a_addr + kk * 2048, 8192, 1024)
-                                        : smem_desc(a_addr + kk * 32, 16, 1024);
-            const uint64_t bdesc = smem_desc(b_addr + kk * 2048, 8192, 1024);
-            mma_bf16(tmem_d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            for (int kk = 0; kk < kBK / 16; ++kk) {
+              const uint64_t adesc = p.kind == VK ? smem_desc(a_addr + kk * 2048, 8192, 1024)
+                                                  : smem_desc(a_addr + kk * 32, 16, 1024);
+              const uint64_t bdesc = smem_desc(b_addr + kk * 2048, 8192, 1024);
+              mma_bf16(tmem_d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
+            }
+            mma_commit_pair(empty0 + 8 * s);
           }
-          mma_commit(empty0 + 8 * s);
+          __syncwarp();
         }
+        if (!ok) break;
+        if (lane == 0) mma_commit_pair(accf0 + 8 * acc);
         __syncwarp();
       }
-      if (!ok) break;
-      if (lane == 0) mma_commit(accf0 + 8 * acc);
+      if (lane == 0) mma_commit_pair(drain);
       __syncwarp();
     }
-    // drain: all MMAs issued by this CTA complete before TMEM is released
-    if (lane == 0) mma_commit(drain);
-    __syncwarp();
+    // drain: all MMAs writing this CTA's TMEM complete before it is released
     mbar_wait(drain, 0, abortv, p.status, false);
   } else {
     // ------------------------------------------------------------ epilogue -----------
@@ -362,8 +414,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     float* stg = reinterpret_cast<float*>(epi + ew * kEpiBytes);
     int lt = 0;
-    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++lt) {
-      const Tile d = decode(p, t);
+    for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
+      const Tile d = decode(p, t, rank);
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
       if (!mbar_wait(accf0 + 8 * acc, acc_ph, abortv, p.status)) break;
       tc_fence_after();
@@ -371,8 +423,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const bool have_acc = d.k_iters > 0;
       const int row_base = p.kind == VK ? d.m0 + q * 32 : d.row0 + q * 32;
       const int row_lim = p.kind == VK ? p.M : d.row_end;
-      const int nrows = min(32, row_lim - row_base);
-      for (int c = half * 4; c < half * 4 + 4; ++c) {
+      const int nrows = d.has_rows ? min(32, row_lim - row_base) : 0;
+      for (int c = half * 4; c < half * 4 + 4 && nrows > 0; ++c) {
         const int n = d.n0 + c * 32;
         if (n >= p.N) break;  // warp-uniform
         uint32_t v[32];
@@ -380,7 +432,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
-        if (nrows <= 0) continue;
 #pragma unroll
         for (int i = 0; i < 32; ++i) stg[lane * kVmLd + i] = __uint_as_float(v[i]);
         __syncwarp();
@@ -453,19 +504,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * acc);
+      if (lane == 0) mbar_arrive_cluster(acce_lead + 8 * acc);
     }
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync_all();  // no multicast or remote arrive may target a CTA that has exited
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
   }
 }
 
-// Tile tables from seg_offsets: plan[0..E] = exclusive prefix of ceil(R_e / kBM) (var-M tiles),
+// Tile tables from seg_offsets: plan[0..E] = exclusive prefix of ceil(R_e / 256) (var-M pair tiles),
 // plan[E+1 .. 2E] = experts ordered by R_e descending, ties by expert id (var-K, longest first).
 // maps[j][e] = template j with its row extent cut at seg_offsets[e+1] (var-K operands).
 struct MapTemplates {
@@ -479,7 +531,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
   const int e = threadIdx.x;
   const int r = e < E ? seg[e + 1] - seg[e] : 0;
   if (e < E) s_r[e] = r;
-  const int mt = (r + kBM - 1) / kBM;
+  const int mt = (r + 2 * kBM - 1) / (2 * kBM);
   // exclusive block scan of mt
   const int lane = e & 31, w = e >> 5;
   int incl = mt;
@@ -568,7 +620,7 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K, uint6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes(int stages) { return 1024 + bar_offset(stages) + (2 * kMaxStages + 5) * 8 + 8; }
+size_t smem_bytes() { return 1024 + bar_offset() + (2 * kStages + 5) * 8 + 8; }
 
 int sm_count() {
   static int n = 0;
@@ -592,16 +644,35 @@ bool device_ok() {
 lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, int64_t tiles_bound,
                       cudaStream_t s) {
   if (tiles_bound <= 0) return LRM_OK;
-  const size_t smem = smem_bytes(p.stages);
+  const size_t smem = smem_bytes();
   static bool attr_set = false;
   if (!attr_set) {
     if (cudaFuncSetAttribute(tc_grouped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem_bytes(kMaxStages)) != cudaSuccess)
+                             (int)smem_bytes()) != cudaSuccess)
       return LRM_ERR_CUDA;
     attr_set = true;
   }
-  const int grid = (int)(tiles_bound < sm_count() ? tiles_bound : sm_count());
-  tc_grouped_kernel<<<grid, kThreads, smem, s>>>(a, b, p);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  static int max_pairs = 0;
+  if (max_pairs == 0) {
+    cfg.gridDim = dim3(2 * sm_count() / 2);
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_kernel, &cfg) != cudaSuccess || n <= 0) n = sm_count() / 2;
+    max_pairs = n;
+  }
+  const int64_t pairs = tiles_bound < max_pairs ? tiles_bound : max_pairs;
+  cfg.gridDim = dim3((unsigned)(2 * pairs));
+  if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel, a, b, p) != cudaSuccess) return LRM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
 }
 
@@ -621,29 +692,29 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
 
   CUtensorMap mA, mB;
-  const int64_t vm_bound = ((int64_t)g.cap + kBM - 1) / kBM + E;
+  const int64_t vm_bound = ((int64_t)g.cap + 2 * kBM - 1) / (2 * kBM) + E;  // pair tiles along M
   lrm_status st;
   // dphi = dy_c W_down[e], SwiGLU backward fused -> dh_c
   if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !make_map_3d(&mB, g.w_down, E, H, I)) return LRM_ERR_CUDA;
-  TcParams p{VM_SWIGLU, kVmStages, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
+  TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
              (const __nv_bfloat16*)g.h_c, g.status, nullptr, nullptr};
   if ((st = launch_one(mA, mB, p, vm_bound * p.nN, s))) return st;
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
-  p = TcParams{VK, kVkStages, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
+  p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
                nullptr, g.status, maps + 0 * E, maps + 1 * E};
   mA = tpl.t[0];
   mB = tpl.t[1];
-  if ((st = launch_one(mA, mB, p, (int64_t)E * p.nM * p.nN, s))) return st;
+  if ((st = launch_one(mA, mB, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
-  p = TcParams{VK, kVkStages, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
+  p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
                g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E};
   mA = tpl.t[2];
   mB = tpl.t[3];
-  if ((st = launch_one(mA, mB, p, (int64_t)E * p.nM * p.nN, s))) return st;
+  if ((st = launch_one(mA, mB, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dx_c = dh_c W_gate_up[e]  (K = 2I, N = H)
   if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !make_map_3d(&mB, g.w_gate_up, E, 2 * I, H))
     return LRM_ERR_CUDA;
-  p = TcParams{VM_STORE, kVmStages, E, 0, H, 2 * I, 0, (H + kBN - 1) / kBN, g.seg_offsets, plan, g.dx_c, nullptr,
+  p = TcParams{VM_STORE, E, 0, H, 2 * I, 0, (H + kBN - 1) / kBN, g.seg_offsets, plan, g.dx_c, nullptr,
                g.status, nullptr, nullptr};
   if ((st = launch_one(mA, mB, p, vm_bound * p.nN, s))) return st;
   return LRM_OK;
