@@ -60,6 +60,9 @@ constexpr int kThreads = 64 + 32 * kEpiWarps;
 // (scalar shared accesses are conflict-free both row-per-thread and row-contiguous).
 constexpr int kVmLd = 33;
 constexpr int kEpiBytes = 32 * kVmLd * 4;
+// var-K: the same region holds one 4 KB, 1024-byte-aligned staging box per warp for TMA stores
+constexpr int kBoxBytes = 4096;
+static_assert(kBoxBytes <= kEpiBytes, "staging box must fit in the per-warp epilogue region");
 constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -163,6 +166,16 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
       : "memory");
 }
+// TMA tensor store from this CTA's shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // A tensor map written by another kernel (generic proxy) must be acquired by the tensormap
 // proxy before a TMA instruction uses it.
 __device__ __forceinline__ void tensormap_acquire(const CUtensorMap* m) {
@@ -276,7 +289,7 @@ __host__ __device__ constexpr uint32_t bar_offset() { return epi_offset() + kEpi
 // ---------------------------------------------------------------- the kernel ---------
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                      const TcParams p) {
+                      const __grid_constant__ CUtensorMap tmC, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int S = kStages;
@@ -412,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (tcgen05.ld 32x32b), staged in shared memory and written back row-contiguous, so global
     // stores (and the SwiGLU h_c loads) are coalesced; var-M rows are masked at the segment end.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
-    float* stg = reinterpret_cast<float*>(epi + ew * kEpiBytes);
+    float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : kEpiBytes));
     int lt = 0;
     for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
       const Tile d = decode(p, t, rank);
@@ -432,24 +445,26 @@ __global__ void __launch_bounds__(kThreads, 1)
         else
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
+        if (p.kind == VK) {
+          // fp32 dW: the warp's 32 x 32 block leaves as one TMA tensor store from a
+          // 128-byte-swizzled staging box (the map clips rows >= M and columns >= N)
+          uint8_t* box = reinterpret_cast<uint8_t*>(stg);
+          if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
+          __syncwarp();
+          uint8_t* line = box + lane * 128;
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj)
+            *reinterpret_cast<uint4*>(line + ((jj ^ (lane & 7)) << 4)) =
+                make_uint4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) tma_store_3d(&tmC, smem_u32(box), n, row_base, d.e);
+          continue;
+        }
 #pragma unroll
         for (int i = 0; i < 32; ++i) stg[lane * kVmLd + i] = __uint_as_float(v[i]);
         __syncwarp();
-        if (p.kind == VK) {
-          // fp32 dW: 4 rows x 128 B per instruction
-          const int sub = lane >> 3, piece = lane & 7;
-          const int col = n + piece * 4;
-          float* out = reinterpret_cast<float*>(p.out) + (int64_t)d.e * p.M * p.N;
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int rr = i * 4 + sub;
-            if (rr < nrows && col < p.N) {
-              const float* sv = stg + rr * kVmLd + piece * 4;
-              *reinterpret_cast<float4*>(out + (int64_t)(row_base + rr) * p.N + col) =
-                  make_float4(sv[0], sv[1], sv[2], sv[3]);
-            }
-          }
-        } else {
+        {
           // bf16 rows: 8 rows x 64 B per instruction; lane owns 8 columns of one row
           const int sub = lane >> 2, piece = lane & 3;
           const int col = n + piece * 8;
@@ -506,6 +521,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(acce_lead + 8 * acc);
     }
+    if (p.kind == VK && lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   }
 
   tc_fence_before();
@@ -620,6 +636,17 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K, uint6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 [E, M, N] output with a {32, 32, 1} box and 128-byte swizzle (the epilogue's staging box).
+bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t N) {
+  const cuuint64_t dims[3] = {N, M, E};
+  const cuuint64_t strides[2] = {N * 4, M * N * 4};
+  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 size_t smem_bytes() { return 1024 + bar_offset() + (2 * kStages + 5) * 8 + 8; }
 
 int sm_count() {
@@ -641,8 +668,8 @@ bool device_ok() {
   return major == 10 && minor == 3;
 }
 
-lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const TcParams& p, int64_t tiles_bound,
-                      cudaStream_t s) {
+lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
+                      int64_t tiles_bound, cudaStream_t s) {
   if (tiles_bound <= 0) return LRM_OK;
   const size_t smem = smem_bytes();
   static bool attr_set = false;
@@ -672,7 +699,7 @@ lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const TcParams
   }
   const int64_t pairs = tiles_bound < max_pairs ? tiles_bound : max_pairs;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
-  if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel, a, b, p) != cudaSuccess) return LRM_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel, a, b, c, p) != cudaSuccess) return LRM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
 }
 
@@ -698,25 +725,28 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !make_map_3d(&mB, g.w_down, E, H, I)) return LRM_ERR_CUDA;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
              (const __nv_bfloat16*)g.h_c, g.status, nullptr, nullptr};
-  if ((st = launch_one(mA, mB, p, vm_bound * p.nN, s))) return st;
+  if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
                nullptr, g.status, maps + 0 * E, maps + 1 * E};
   mA = tpl.t[0];
   mB = tpl.t[1];
-  if ((st = launch_one(mA, mB, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
+  CUtensorMap mC;
+  if (!make_map_out3d(&mC, g.dw_down, E, H, I)) return LRM_ERR_CUDA;
+  if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
   p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
                g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E};
   mA = tpl.t[2];
   mB = tpl.t[3];
-  if ((st = launch_one(mA, mB, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
+  if (!make_map_out3d(&mC, g.dw_gate_up, E, 2 * I, H)) return LRM_ERR_CUDA;
+  if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dx_c = dh_c W_gate_up[e]  (K = 2I, N = H)
   if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !make_map_3d(&mB, g.w_gate_up, E, 2 * I, H))
     return LRM_ERR_CUDA;
   p = TcParams{VM_STORE, E, 0, H, 2 * I, 0, (H + kBN - 1) / kBN, g.seg_offsets, plan, g.dx_c, nullptr,
                g.status, nullptr, nullptr};
-  if ((st = launch_one(mA, mB, p, vm_bound * p.nN, s))) return st;
+  if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   return LRM_OK;
 }
 
