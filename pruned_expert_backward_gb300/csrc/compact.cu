@@ -11,7 +11,7 @@
 // scaled by alpha_u) into each kept pair's row; the token's k rows of h and phi are one
 // contiguous span, read only where the pair is kept.  16-byte coalesced loads and stores.
 //
-// scatter_dx: a CTA covers several tokens (up to 1024 threads); each thread owns one 16-byte
+// scatter_dx: a CTA covers several tokens (up to 512 threads); each thread owns one 16-byte
 // column slice of one token, issues the k row loads together and adds them in j order in
 // fp32 (deterministic, no atomics).
 #include "common.cuh"
@@ -84,16 +84,16 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   }
 }
 
-template <typename T>
-__global__ void __launch_bounds__(1024) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
+template <typename T, int MAXK>
+__global__ void __launch_bounds__(512, MAXK <= 8 ? 2 : 1) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
                                                           const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
                                                           int tok_per_blk, T* __restrict__ dx) {
   constexpr int VN = VecTraits<T>::N;
-  extern __shared__ int64_t s_rows[];  // [tok_per_blk][k]
+  extern __shared__ int32_t s_rows[];  // [tok_per_blk][k]
   const int64_t t0 = (int64_t)blockIdx.x * tok_per_blk;
   for (int i = threadIdx.x; i < tok_per_blk * k; i += blockDim.x) {
     const int64_t u = t0 * k + i;
-    s_rows[i] = u < n_tok * k ? (int64_t)row_of_pair[u] : -1;
+    s_rows[i] = u < n_tok * k ? row_of_pair[u] : -1;
   }
   __syncthreads();
   const int nvH = H / VN;
@@ -101,18 +101,21 @@ __global__ void __launch_bounds__(1024) scatter_dx_kernel(const int32_t* __restr
     const int tt = w / nvH, v = w - tt * nvH;
     const int64_t t = t0 + tt;
     if (t >= n_tok) break;
-    const int64_t* rows = s_rows + tt * k;
-    uint4 vals[LRM_MAX_TOPK];
+    const int32_t* srow = s_rows + tt * k;
+    int32_t rows[MAXK];
 #pragma unroll
-    for (int j = 0; j < LRM_MAX_TOPK; ++j) {
-      if (j < k && rows[j] >= 0) vals[j] = ld_stream16(dx_c + rows[j] * H + v * VN);
+    for (int j = 0; j < MAXK; ++j) rows[j] = j < k ? srow[j] : -1;
+    uint4 vals[MAXK];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+      if (rows[j] >= 0) vals[j] = ld_stream16(dx_c + (int64_t)rows[j] * H + v * VN);
     }
     float acc[VN];
 #pragma unroll
     for (int q = 0; q < VN; ++q) acc[q] = 0.f;
 #pragma unroll
-    for (int j = 0; j < LRM_MAX_TOPK; ++j) {
-      if (j < k && rows[j] >= 0) {
+    for (int j = 0; j < MAXK; ++j) {
+      if (rows[j] >= 0) {
         float f[VN];
         unpack(vals[j], f);
 #pragma unroll
@@ -124,7 +127,7 @@ __global__ void __launch_bounds__(1024) scatter_dx_kernel(const int32_t* __restr
 }
 
 int threads_for(int n_vec) {
-  int t = n_vec < 1024 ? n_vec : 1024;
+  int t = n_vec < 512 ? n_vec : 512;
   t = (t + 31) / 32 * 32;
   return t < 32 ? 32 : t;
 }
@@ -151,18 +154,23 @@ void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, 
                        void* dx, cudaStream_t s) {
   if (T == 0) return;
   const int nvH = H / (dt == LRM_BF16 ? 8 : 4);
-  int tok = nvH >= 1024 ? 1 : 1024 / nvH;  // one thread per 16-byte column slice, up to 1024 threads
+  int tok = nvH >= 512 ? 1 : 512 / nvH;  // one thread per 16-byte column slice, up to 512 threads
   if (tok > 64) tok = 64;
   const int threads = threads_for(nvH * tok);
   const unsigned blocks = (unsigned)((T + tok - 1) / tok);
-  const size_t smem = sizeof(int64_t) * tok * k;
-  if (dt == LRM_BF16) {
-    using B = __nv_bfloat16;
-    scatter_dx_kernel<B><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok, (B*)dx);
-  } else {
-    scatter_dx_kernel<float><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H, tok,
-                                                           (float*)dx);
-  }
+  const size_t smem = sizeof(int32_t) * tok * k;
+  using B = __nv_bfloat16;
+  if (dt == LRM_BF16 && k <= 8)
+    scatter_dx_kernel<B, 8><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok, (B*)dx);
+  else if (dt == LRM_BF16)
+    scatter_dx_kernel<B, LRM_MAX_TOPK><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok,
+                                                                     (B*)dx);
+  else if (k <= 8)
+    scatter_dx_kernel<float, 8><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H, tok,
+                                                              (float*)dx);
+  else
+    scatter_dx_kernel<float, LRM_MAX_TOPK><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H,
+                                                                         tok, (float*)dx);
 }
 
 }  // namespace lrm

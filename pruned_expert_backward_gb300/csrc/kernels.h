@@ -10,9 +10,8 @@
 
 namespace lrm {
 
-// Selection works on warp-sized chunks of this many consecutive pairs.
+// Selection works on chunks of this many consecutive pairs (one CTA, one pair per thread).
 constexpr int kSelChunk = 256;
-constexpr int kSelWarpsPerBlock = 8;
 
 struct SelectWs {
   int32_t* counts;        // [n_chunks][E]  per-chunk expert counts, then exclusive bases

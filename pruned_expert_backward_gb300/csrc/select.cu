@@ -5,13 +5,14 @@
 // the smaller pair index u; inside a segment the kept pairs are listed in u order.
 //
 // Four launches, all deterministic:
-//  1. count:   each warp owns a chunk of kSelChunk consecutive pairs and counts its experts.
+//  1. count:   one CTA per chunk of kSelChunk consecutive pairs counts the chunk's experts.
 //  2. scan:    one CTA per expert: exclusive scan of that expert's chunk counts (bucket
 //              bases inside the expert's bucket) and its load.
-//  3. bucket:  every CTA derives the expert-level prefixes (bucket starts, kept counts
+//  3. bucket:  one CTA per chunk derives the expert-level prefixes (bucket starts, kept counts
 //              min(quota, load), segment offsets, capacity check; CTA 0 publishes them),
-//              then scatters its chunks' pairs stably into the expert buckets (u ascending)
-//              with their score bits; ranks within a warp come from __match_any_sync.
+//              then scatters its pairs stably into the expert buckets (u ascending) with
+//              their score bits: ranks within a warp from __match_any_sync, across warps from
+//              per-warp expert counts.
 //  4. expert:  one CTA per expert: MSD radix select (4 x 8 bits) of the quota-th largest
 //              score in the bucket, then one ordered pass that keeps everything above the
 //              threshold plus the first `need` pairs equal to it, and writes kept_pair and
@@ -54,26 +55,21 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sm) {
   return res;
 }
 
-__global__ void __launch_bounds__(256) sel_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
-                                                        int64_t n_chunks, int32_t* __restrict__ counts,
-                                                        int32_t* status) {
-  extern __shared__ int hist[];  // [kSelWarpsPerBlock][E]
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  int* h = hist + warp * E;
-  for (int e = lane; e < E; e += 32) h[e] = 0;
-  __syncwarp();
-  const int64_t c = (int64_t)blockIdx.x * kSelWarpsPerBlock + warp;
-  if (c >= n_chunks) return;
-  const int64_t u0 = c * kSelChunk, u1 = min(P, u0 + kSelChunk);
-  for (int64_t u = u0 + lane; u < u1; u += 32) {
-    const int e = idx[u];
-    if (e >= 0 && e < E)
-      atomicAdd(&h[e], 1);
-    else
-      set_status(status, LRM_ERR_BAD_INDEX);
-  }
-  __syncwarp();
-  for (int e = lane; e < E; e += 32) counts[c * E + e] = h[e];
+__global__ void __launch_bounds__(kSelChunk) sel_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
+                                                              int32_t* __restrict__ counts, int32_t* status) {
+  extern __shared__ int hist[];  // [E]
+  for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int64_t c = blockIdx.x;
+  const int64_t u = c * kSelChunk + threadIdx.x;
+  const int e = u < P ? idx[u] : -1;
+  const bool good = u < P && e >= 0 && e < E;
+  if (u < P && !good) set_status(status, LRM_ERR_BAD_INDEX);
+  // warp-aggregated: one shared atomic per distinct expert in the warp
+  const unsigned peers = __match_any_sync(0xffffffffu, good ? e : -1);
+  if (good && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+  __syncthreads();
+  for (int e = threadIdx.x; e < E; e += blockDim.x) counts[c * E + e] = hist[e];
 }
 
 // One CTA per expert: exclusive scan down the expert's column of chunk counts.
@@ -97,25 +93,36 @@ __global__ void __launch_bounds__(1024) sel_colscan_kernel(int32_t* __restrict__
   if (threadIdx.x == 0) loads[e] = s_run;
 }
 
-__global__ void __launch_bounds__(256) sel_bucket_kernel(
+__global__ void __launch_bounds__(kSelChunk) sel_bucket_kernel(
     const int32_t* __restrict__ idx, const float* __restrict__ scores, int64_t P, int E, int64_t n_chunks,
     const int32_t* __restrict__ counts, const int32_t* __restrict__ loads, const int32_t* __restrict__ quotas,
     int64_t cap, int32_t* __restrict__ bucket_start, int32_t* __restrict__ keep, int32_t* __restrict__ seg_offsets,
     int32_t* __restrict__ sorted_u, uint32_t* __restrict__ sorted_key, int32_t* __restrict__ row_of_pair,
     int32_t* status) {
+  constexpr int kWarps = kSelChunk / 32;
   extern __shared__ int sh[];
-  int* s_bstart = sh;                       // [E]
-  int* run_all = sh + E;                    // [kSelWarpsPerBlock][E]
+  int* s_base = sh;              // [E]  this chunk's first slot of each expert
+  int* s_wcnt = sh + E;          // [kWarps][E] per-warp counts, then per-warp exclusive offsets
+  int* s_seg = sh + E + kWarps * E;  // [E] segment starts (block 0 publishes)
   __shared__ int sm[33];
   __shared__ int s_base_l, s_base_k, s_overflow;
-  const int tid = threadIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int64_t c = blockIdx.x;
 
-  // expert-level prefixes (E <= 1024: at most 4 experts per thread, processed in order)
+  // this thread's pair (issued first so its latency overlaps the prefix work below)
+  const int64_t u = c * kSelChunk + tid;
+  const bool valid = u < P;
+  const int e_raw = valid ? idx[u] : -1;
+  const bool good = valid && e_raw >= 0 && e_raw < E;
+  const uint32_t key = good ? __float_as_uint(scores[u]) : 0u;
+
+  // expert-level prefixes: bucket starts, kept counts, segment offsets (E <= 1024)
   if (tid == 0) { s_base_l = 0; s_base_k = 0; }
+  for (int i = tid; i < kWarps * E; i += kSelChunk) s_wcnt[i] = 0;
   __syncthreads();
   int kp_mine[4];
-  for (int r = 0; r < (E + 255) / 256; ++r) {
-    const int e = r * 256 + tid;
+  for (int r = 0; r < (E + kSelChunk - 1) / kSelChunk; ++r) {
+    const int e = r * kSelChunk + tid;
     const int l = e < E ? loads[e] : 0;
     int kp = 0;
     if (e < E) {
@@ -127,8 +134,8 @@ __global__ void __launch_bounds__(256) sel_bucket_kernel(
     const int xl = block_excl_scan(l, &tl, sm);
     const int xk = block_excl_scan(kp, &tk, sm);
     if (e < E) {
-      s_bstart[e] = s_base_l + xl;
-      run_all[e] = s_base_k + xk;  // temporarily: segment start
+      s_base[e] = s_base_l + xl + (c < n_chunks ? counts[c * E + e] : 0);
+      s_seg[e] = s_base_k + xk;
     }
     __syncthreads();
     if (tid == 0) { s_base_l += tl; s_base_k += tk; }
@@ -138,12 +145,12 @@ __global__ void __launch_bounds__(256) sel_bucket_kernel(
   __syncthreads();
   const bool overflow = s_overflow;
   if (blockIdx.x == 0) {
-    for (int r = 0; r < (E + 255) / 256; ++r) {
-      const int e = r * 256 + tid;
+    for (int r = 0; r < (E + kSelChunk - 1) / kSelChunk; ++r) {
+      const int e = r * kSelChunk + tid;
       if (e < E) {
-        bucket_start[e] = s_bstart[e];
+        bucket_start[e] = s_base[e];  // block 0 is chunk 0, whose offset inside every bucket is 0
         keep[e] = overflow ? 0 : kp_mine[r];
-        seg_offsets[e] = overflow ? 0 : run_all[e];
+        seg_offsets[e] = overflow ? 0 : s_seg[e];
       }
     }
     if (tid == 0) {
@@ -152,36 +159,26 @@ __global__ void __launch_bounds__(256) sel_bucket_kernel(
       if (overflow) set_status(status, LRM_ERR_CAPACITY);
     }
   }
-  __syncthreads();
 
-  // stable scatter of this block's chunks
-  const int warp = tid >> 5, lane = tid & 31;
-  const int64_t c = (int64_t)blockIdx.x * kSelWarpsPerBlock + warp;
-  if (c >= n_chunks) return;
-  int* run = run_all + warp * E;
-  for (int e = lane; e < E; e += 32) run[e] = s_bstart[e] + counts[c * E + e];
-  __syncwarp();
-  const unsigned lt = (1u << lane) - 1u;
-  const int64_t u0 = c * kSelChunk, u1 = min(P, u0 + kSelChunk);
-  for (int64_t base = u0; base < u1; base += 32) {
-    const int64_t u = base + lane;
-    const bool valid = u < u1;
-    int e = valid ? idx[u] : -1;
-    const bool good = valid && e >= 0 && e < E;
-    const uint32_t key = good ? __float_as_uint(scores[u]) : 0u;
-    if (valid && !good) row_of_pair[u] = -1;
-    const int grp = good ? e : -1;
-    const unsigned peers = __match_any_sync(0xffffffffu, grp);
-    int rank = 0;
-    if (good) {
-      rank = __popc(peers & lt);
-      const int pos = run[e] + rank;
-      sorted_u[pos] = (int32_t)u;
-      sorted_key[pos] = key;
+  // stable rank of this pair among the chunk's pairs of the same expert (u order)
+  const unsigned peers = __match_any_sync(0xffffffffu, good ? e_raw : -1);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (good && rank_w == 0) s_wcnt[warp * E + e_raw] = __popc(peers);
+  __syncthreads();
+  for (int e = tid; e < E; e += kSelChunk) {  // per expert: exclusive offsets over the warps
+    int run = 0;
+    for (int w = 0; w < kWarps; ++w) {
+      const int v = s_wcnt[w * E + e];
+      s_wcnt[w * E + e] = run;
+      run += v;
     }
-    __syncwarp();
-    if (good && rank == 0) run[e] += __popc(peers);
-    __syncwarp();
+  }
+  __syncthreads();
+  if (valid && !good) row_of_pair[u] = -1;
+  if (good) {
+    const int pos = s_base[e_raw] + s_wcnt[warp * E + e_raw] + rank_w;
+    sorted_u[pos] = (int32_t)u;
+    sorted_key[pos] = key;
   }
 }
 
@@ -227,10 +224,22 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
     if (tid < 256) hist[tid] = 0;
     __syncthreads();
-#pragma unroll 4
-    for (int i = tid; i < load; i += kExpThreads) {
-      const uint32_t key = bk[i];
-      if ((key & hi_mask) == prefix) atomicAdd(&hist[(key >> shift) & 255u], 1);
+    for (int i0 = 0; i0 < load; i0 += kExpThreads * 8) {  // warp-uniform trip count
+      uint32_t keys[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {  // all eight loads in flight before any is used
+        const int i = i0 + q * kExpThreads + tid;
+        keys[q] = i < load ? bk[i] : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * kExpThreads + tid;
+        const bool in = i < load && (keys[q] & hi_mask) == prefix;
+        const int bin = in ? (int)((keys[q] >> shift) & 255u) : -1;
+        // scores cluster in a few bins: aggregate per warp before touching shared memory
+        const unsigned peers = __match_any_sync(0xffffffffu, bin);
+        if (in && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+      }
     }
     __syncthreads();
     // suffix counts over bins, highest bin first: thread b' handles bin 255 - b'
@@ -301,11 +310,11 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
                    int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair, const SelectWs& ws,
                    int32_t* status, cudaStream_t s) {
   const int64_t nc = ws.n_chunks;
-  const unsigned cblocks = (unsigned)((nc + kSelWarpsPerBlock - 1) / kSelWarpsPerBlock);
-  const size_t smem = (size_t)kSelWarpsPerBlock * E * sizeof(int);
-  if (nc > 0) sel_count_kernel<<<cblocks, 32 * kSelWarpsPerBlock, smem, s>>>(topk_idx, P, E, nc, ws.counts, status);
+  if (nc > 0)
+    sel_count_kernel<<<(unsigned)nc, kSelChunk, E * sizeof(int), s>>>(topk_idx, P, E, ws.counts, status);
   sel_colscan_kernel<<<E, 1024, 0, s>>>(ws.counts, nc, E, ws.loads);
-  sel_bucket_kernel<<<cblocks > 0 ? cblocks : 1, 32 * kSelWarpsPerBlock, smem + E * sizeof(int), s>>>(
+  const size_t bsmem = (size_t)(2 + kSelChunk / 32) * E * sizeof(int);
+  sel_bucket_kernel<<<nc > 0 ? (unsigned)nc : 1u, kSelChunk, bsmem, s>>>(
       topk_idx, scores, P, E, nc, ws.counts, ws.loads, quotas, cap, ws.bucket_start, ws.keep, seg_offsets,
       ws.sorted_u, ws.sorted_key, row_of_pair, status);
   if (P > 0)
