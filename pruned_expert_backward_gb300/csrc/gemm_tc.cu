@@ -112,10 +112,10 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 // Bounded wait.  Returns false (and raises the abort flag) when the barrier does not
-// complete within kWaitNs, or when another role of the CTA has already aborted.
-__device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
-                                       bool honour_abort = true) {
-  if (mbar_try(bar, parity)) return true;
+// complete within kWaitNs, or when another role of the CTA has already aborted.  The common
+// case (already complete) stays inline; the polling loop is out of line.
+__device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                            int32_t* status, bool honour_abort) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try(bar, parity)) return true;
@@ -127,6 +127,11 @@ __device__ __noinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile i
   *abort_flag = 1;
   set_status(status, LRM_ERR_TIMEOUT);
   return false;
+}
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int32_t* status,
+                                          bool honour_abort = true) {
+  if (mbar_try(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status, honour_abort);
 }
 // Cluster helpers.  CTAs run in pairs (a cluster of two); the even CTA is the MMA leader.
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -335,7 +340,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Both CTAs load their own 128 rows of A and their own 128 columns of B; the loads
     // complete on the leader's full barrier, which the leader's MMA waits on.
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t it = 0, st = 0, sph = 0;  // iteration count, its stage and phase
       bool ok = true;
       int last_e = -1;
       for (int t = pair; t < n_tiles && ok; t += n_pairs) {
@@ -353,7 +358,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         const int nb = d.n0 + rank * (kBN / 2);  // this CTA's half of the B columns
         for (int kb = 0; kb < d.k_iters; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
+          const uint32_t s = st, ph = sph;
+          if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
           if (!mbar_wait(empty0 + 8 * s, ph ^ 1u, abortv, p.status)) { ok = false; break; }
           const uint32_t a_dst = smem_u32(smem + s * kStageBytes), b_dst = a_dst + kABytes;
           const uint32_t fb = full_lead + 8 * s;
@@ -383,7 +389,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // both CTAs' shared memory into both CTAs' TMEM (128 rows each).
     if (leader) {
       const uint32_t idesc = instr_desc(p.kind == VK ? 1u : 0u, 1u);
-      uint32_t it = 0;
+      uint32_t st = 0, sph = 0;
       int lt = 0;
       bool ok = true;
       for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
@@ -392,8 +398,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
         tc_fence_after();
         const uint32_t tmem_d = tmem_base + acc * kBN;
-        for (int kb = 0; kb < d.k_iters; ++kb, ++it) {
-          const uint32_t s = it % S, ph = (it / S) & 1u;
+        for (int kb = 0; kb < d.k_iters; ++kb) {
+          const uint32_t s = st, ph = sph;
+          if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
           if (!mbar_wait(full0 + 8 * s, ph, abortv, p.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
