@@ -387,8 +387,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------ MMA issuer ---------
     // Only the leader issues: tcgen05.mma.cta_group::2 computes the 256 x 256 pair tile from
     // both CTAs' shared memory into both CTAs' TMEM (128 rows each).
-    if (leader) {
+    if (leader && lane == 0) {
       const uint32_t idesc = instr_desc(p.kind == VK ? 1u : 0u, 1u);
+      // descriptors of stage 0; a stage or a 16-deep K step is a constant offset in the address
+      // field (addresses stay below 256 KB, so the 14-bit field never carries)
+      const uint32_t a0 = smem_u32(smem), b0 = a0 + kABytes;
+      const uint64_t adesc0 = p.kind == VK ? smem_desc(a0, 8192, 1024) : smem_desc(a0, 16, 1024);
+      const uint64_t bdesc0 = smem_desc(b0, 8192, 1024);
+      const uint64_t a_kstep = p.kind == VK ? (2048 >> 4) : (32 >> 4), b_kstep = 2048 >> 4;
       uint32_t st = 0, sph = 0;
       int lt = 0;
       bool ok = true;
@@ -403,26 +409,19 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
           if (!mbar_wait(full0 + 8 * s, ph, abortv, p.status)) { ok = false; break; }
           tc_fence_after();
-          if (lane == 0) {
-            const uint32_t a_addr = smem_u32(smem + s * kStageBytes), b_addr = a_addr + kABytes;
+          const uint64_t soff = (uint64_t)((s * kStageBytes) >> 4);
 #pragma unroll
-            for (int kk = 0; kk < kBK / 16; ++kk) {
-              const uint64_t adesc = p.kind == VK ? smem_desc(a_addr + kk * 2048, 8192, 1024)
-                                                  : smem_desc(a_addr + kk * 32, 16, 1024);
-              const uint64_t bdesc = smem_desc(b_addr + kk * 2048, 8192, 1024);
-              mma_bf16(tmem_d, adesc, bdesc, idesc, (kb | kk) != 0 ? 1u : 0u);
-            }
-            mma_commit_pair(empty0 + 8 * s);
-          }
-          __syncwarp();
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_bf16(tmem_d, adesc0 + soff + kk * a_kstep, bdesc0 + soff + kk * b_kstep, idesc,
+                     (kb | kk) != 0 ? 1u : 0u);
+          mma_commit_pair(empty0 + 8 * s);
         }
         if (!ok) break;
-        if (lane == 0) mma_commit_pair(accf0 + 8 * acc);
-        __syncwarp();
+        mma_commit_pair(accf0 + 8 * acc);
       }
-      if (lane == 0) mma_commit_pair(drain);
-      __syncwarp();
+      mma_commit_pair(drain);
     }
+    __syncwarp();
     // drain: all MMAs writing this CTA's TMEM complete before it is released
     mbar_wait(drain, 0, abortv, p.status, false);
   } else {
