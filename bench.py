@@ -76,6 +76,23 @@ def algorithmic(wl, R, T_any):
     }
 
 
+# ------------------------------------------------------------------ ranks -----------------
+def aggregate_over_ranks(ms, retained, dist=None, device="cpu"):
+    """Whole-job view of one timed region: the slowest rank's milliseconds and the retained
+    pairs of all ranks (each rank runs its own batch; no data moves between ranks)."""
+    if dist is None:
+        return float(ms), float(retained)
+    t = torch.tensor([float(ms)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    r = torch.tensor([float(retained)], dtype=torch.float64, device=device)
+    dist.all_reduce(r)
+    return float(t.item()), float(r.item())
+
+
+def pairs_per_second(retained_total, steps, ms):
+    return retained_total * steps / (ms / 1e3)
+
+
 # ------------------------------------------------------------------ clocks ----------------
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -272,23 +289,14 @@ def main():
     if pg:
         pg.barrier()
     clk = clocks.stop()
-    total_ms = t_start.elapsed_time(t_end)
-    if pg:
-        t = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        total_ms = float(t.item())
-        r_all = torch.tensor([R], device=dev, dtype=torch.float64)
-        pg.all_reduce(r_all)
-        R_total = float(r_all.item())
-    else:
-        R_total = float(R)
+    total_ms, R_total = aggregate_over_ranks(t_start.elapsed_time(t_end), R, pg, dev)
     stage_ms = {s: 0.0 for s in stages}
     for e in evs:
         for j, s in enumerate(stages):
             stage_ms[s] += e[j].elapsed_time(e[j + 1])
     stage_ms = {s: v / args.steps for s, v in stage_ms.items()}
     ms_per_step = total_ms / args.steps
-    value = R_total * args.steps / (total_ms / 1e3)
+    value = pairs_per_second(R_total, args.steps, total_ms)
 
     # ---- end-to-end through the public API with pinned host buffers ------------------------
     e2e = end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev)
@@ -398,12 +406,8 @@ def end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev):
         one()
     b.record(stream)
     torch.cuda.synchronize()
-    ms = a.elapsed_time(b)
-    if pg:
-        t = torch.tensor([ms], device=dev)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
-    return {"value": round(R_total * steps / (ms / 1e3), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
+    ms, _ = aggregate_over_ranks(a.elapsed_time(b), 0, pg, dev)
+    return {"value": round(pairs_per_second(R_total, steps, ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4)}
 
 

@@ -179,6 +179,17 @@ lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t 
                           lrm_dtype dt, void* dx, cudaStream_t stream);
 
 /*
+ * Self-test of failure detection (no counterpart in the pages; part of this library's fault
+ * handling).  The tensor-core kernels bound every wait on an mbarrier (about one second of
+ * %globaltimer): on expiry they record LRM_ERR_TIMEOUT, drain their in-flight copies and MMAs,
+ * free TMEM and return, so a stalled pipeline never hangs the GPU.  This entry point runs that
+ * same wait routine on an mbarrier that nothing ever arrives on, with the limit `limit_ns`
+ * (0 < limit_ns <= 1e10): the kernel returns after about limit_ns and writes LRM_ERR_TIMEOUT to
+ * *dev_status (device memory, caller zeroes it).  Errors: LRM_ERR_INVALID_ARG, LRM_ERR_CUDA.
+ */
+lrm_status lrm_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns, cudaStream_t stream);
+
+/*
  * lrm_select_static — lrm_select for callers that cannot allocate device memory.
  * The LRMoE pages have no counterpart: this is a deployment convenience of this library.
  *

@@ -29,6 +29,7 @@ SIGNATURES = {
     "lrm_grouped_backward": (C.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, C.c_int, _i64, _p, _p,
                                        _p, _p, _p, _sz, _i32, _p, _p]),
     "lrm_scatter_dx": (C.c_int, [_p, _p, _i64, _i32, _i32, C.c_int, _p, _p]),
+    "lrm_selftest_wait_timeout": (C.c_int, [_p, _i64, _p]),
 }
 
 _lib = None

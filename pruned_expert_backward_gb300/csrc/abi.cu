@@ -192,4 +192,9 @@ lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t 
   return after_launch();
 }
 
+lrm_status lrm_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns, cudaStream_t stream) {
+  if (!dev_status || limit_ns <= 0 || limit_ns > 10000000000ll) return LRM_ERR_INVALID_ARG;
+  return launch_wait_selftest(dev_status, limit_ns, stream);
+}
+
 }  // extern "C"

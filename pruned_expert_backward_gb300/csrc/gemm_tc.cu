@@ -115,13 +115,13 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
 // complete within kWaitNs, or when another role of the CTA has already aborted.  The common
 // case (already complete) stays inline; the polling loop is out of line.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            int32_t* status, bool honour_abort) {
+                                            int32_t* status, bool honour_abort, uint64_t limit_ns = kWaitNs) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
     if (mbar_try(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (honour_abort && *abort_flag) return false;
-      if (globaltimer() - t0 > kWaitNs) break;
+      if (globaltimer() - t0 > limit_ns) break;
     }
   }
   *abort_flag = 1;
@@ -601,6 +601,19 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
   }
 }
 
+// Self-test of the bounded wait: one thread waits on an mbarrier that nothing will ever arrive
+// on.  The wait must give up after `limit_ns`, record LRM_ERR_TIMEOUT and return normally.
+__global__ void wait_selftest_kernel(int32_t* status, uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  const uint32_t b = smem_u32(&bar);
+  mbar_init(b, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  mbar_wait_slow(b, 0, &abort_flag, status, true, limit_ns);  // phase 0 never completes
+}
+
 // ---------------------------------------------------------------- host side ----------
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -710,6 +723,11 @@ lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
 }
 
 }  // namespace
+
+lrm_status launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s) {
+  wait_selftest_kernel<<<1, 32, 0, s>>>(status, (uint64_t)limit_ns);
+  return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
+}
 
 lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_t s) {
   if (!device_ok() || encode_fn() == nullptr) return LRM_ERR_UNSUPPORTED;

@@ -67,5 +67,6 @@ struct GroupedArgs {
 void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s);
 // Returns LRM_OK, or LRM_ERR_UNSUPPORTED / LRM_ERR_CUDA when the tensor-core path cannot run.
 lrm_status launch_grouped_tc(const GroupedArgs& a, const GemmWs& ws, cudaStream_t s);
+lrm_status launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s);
 
 }  // namespace lrm

@@ -205,3 +205,21 @@ def test_nonfinite_score_flags():
     lrm.lrm_score(inp["alpha"], inp["g"], inp["phi"], dev_status=st)
     torch.cuda.synchronize()
     assert int(st.item()) == 7  # LRM_ERR_NONFINITE
+
+
+def test_bounded_wait_times_out_and_context_survives():
+    """Failure detection without a fault: a wait that nothing satisfies gives up, reports
+    LRM_ERR_TIMEOUT in the status word, and the GPU keeps working afterwards."""
+    import time
+    from pruned_expert_backward_gb300 import _lib
+    lib = _lib.load()
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    t0 = time.perf_counter()
+    assert lib.lrm_selftest_wait_timeout(st.data_ptr(), 20_000_000, torch.cuda.current_stream().cuda_stream) == 0
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    assert int(st.item()) == 8  # LRM_ERR_TIMEOUT
+    assert 0.015 <= dt < 2.0
+    wl = W.small_workload("after_timeout", 256, 256, 128, 8, 2)
+    inp, loads, q, pb = run_cuda_path(wl, flags=TC)
+    full_check(wl, inp, loads, q, pb)
