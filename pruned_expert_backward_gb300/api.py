@@ -201,3 +201,65 @@ class PrunedBackward:
                 "row_of_pair": self.row_of_pair, "dy_c": self.dy_c, "x_c": self.x_c, "h_c": self.h_c,
                 "phi_c": self.phi_c, "dh_c": self.dh_c, "dx_c": self.dx_c, "dw_gate_up": self.dw_gate_up,
                 "dw_down": self.dw_down, "dx": self.dx, "dev_status": self.dev_status}
+
+
+class HostPipeline:
+    """The pruned backward over batches held in pinned host memory.
+
+    Two device copies of the per-step inputs (topk_idx, alpha, x, g, h, phi and the quotas) are
+    kept: while step i computes on the current stream, step i+1's inputs travel host -> device on
+    a copy stream into the other copy, so transfers overlap compute.  After every step
+    its result (dX and seg_offsets) is copied back to pinned host buffers and the host waits for
+    it.  The weights stay on the device.  All compute runs in liblrm.so's kernels (through
+    PrunedBackward); this class only orders copies with CUDA events."""
+
+    NAMES = ("topk_idx", "alpha", "x", "g", "h", "phi")
+
+    def __init__(self, pb: PrunedBackward, w_gate_up, w_down):
+        self.pb = pb
+        self.w_gate_up, self.w_down = w_gate_up, w_down
+        self.copy_stream = torch.cuda.Stream(device=w_down.device)
+        self.sets = [None, None]
+        self.quotas = [None, None]
+        self.ready = [torch.cuda.Event(), torch.cuda.Event()]
+        self.free = [torch.cuda.Event(), torch.cuda.Event()]
+        self.dx_host = torch.empty(pb.dx.shape, dtype=pb.dx.dtype).pin_memory()
+        self.seg_host = torch.empty(pb.seg_offsets.shape, dtype=torch.int32).pin_memory()
+
+    def _upload(self, slot, host_inp, host_quotas):
+        if self.sets[slot] is None:
+            self.sets[slot] = {n: torch.empty(host_inp[n].shape, dtype=host_inp[n].dtype,
+                                              device=self.w_down.device) for n in self.NAMES}
+            self.quotas[slot] = torch.empty(host_quotas.shape, dtype=torch.int32, device=self.w_down.device)
+        with torch.cuda.stream(self.copy_stream):
+            self.copy_stream.wait_event(self.free[slot])  # the step that last used this slot is done
+            for n in self.NAMES:
+                self.sets[slot][n].copy_(host_inp[n], non_blocking=True)
+            self.quotas[slot].copy_(host_quotas, non_blocking=True)
+            self.ready[slot].record(self.copy_stream)
+
+    def run(self, batches, on_result=None):
+        """batches: a list of (host_inputs dict, host_quotas int32 [E]) in pinned memory.
+        Returns the retained row count of each step (read from the step's seg_offsets).
+        on_result(i, dx_host, seg_offsets_host), if given, sees each step's result on the host
+        (the buffers are reused by the next step)."""
+        retained = []
+        if not batches:
+            return retained
+        cur = torch.cuda.current_stream()
+        self._upload(0, *batches[0])
+        for i in range(len(batches)):
+            slot = i & 1
+            if i + 1 < len(batches):
+                self._upload(slot ^ 1, *batches[i + 1])
+            cur.wait_event(self.ready[slot])
+            inp = dict(self.sets[slot], w_gate_up=self.w_gate_up, w_down=self.w_down)
+            self.pb.run(inp, self.quotas[slot])
+            self.free[slot].record(cur)
+            self.dx_host.copy_(self.pb.dx, non_blocking=True)
+            self.seg_host.copy_(self.pb.seg_offsets, non_blocking=True)
+            cur.synchronize()
+            retained.append(int(self.seg_host[-1]))
+            if on_result is not None:
+                on_result(i, self.dx_host, self.seg_host)
+        return retained

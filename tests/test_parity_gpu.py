@@ -223,3 +223,29 @@ def test_bounded_wait_times_out_and_context_survives():
     wl = W.small_workload("after_timeout", 256, 256, 128, 8, 2)
     inp, loads, q, pb = run_cuda_path(wl, flags=TC)
     full_check(wl, inp, loads, q, pb)
+
+
+def test_host_pipeline_matches_device_path():
+    """Pinned-host batches through HostPipeline (copies overlapping compute) give, step after
+    step, exactly the results of the device-resident path."""
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.small_workload("host_pipe", 600, 256, 128, 16, 4)
+    w = W.generate(wl, "cuda", seed=3)
+    refs, batches = [], []
+    for seed in (3, 4, 5):
+        inp = W.generate(wl, "cuda", seed=seed)
+        inp["w_gate_up"], inp["w_down"] = w["w_gate_up"], w["w_down"]
+        _, q = lrm.lrm_plan_quotas(inp["topk_idx"], wl.E, "ratio", 8, 10)
+        pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I)
+        pb.run(inp, q)
+        torch.cuda.synchronize()
+        refs.append((pb.dx.cpu().clone(), pb.seg_offsets.cpu().clone()))
+        batches.append(({n: inp[n].cpu().pin_memory() for n in lrm.HostPipeline.NAMES}, q.cpu().pin_memory()))
+    pipe = lrm.HostPipeline(lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I), w["w_gate_up"], w["w_down"])
+    seen = []
+    got = pipe.run(batches + batches[::-1], on_result=lambda i, dx, seg: seen.append((dx.clone(), seg.clone())))
+    order = [0, 1, 2, 2, 1, 0]
+    assert got == [int(refs[j][1][-1]) for j in order]
+    for (dx, seg), j in zip(seen, order):
+        assert torch.equal(seg, refs[j][1])
+        assert torch.equal(dx, refs[j][0])
