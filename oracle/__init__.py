@@ -2,6 +2,7 @@
 
 Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline / reference arm use it.
 """
-from .lrm_oracle import (compact, expert_backward, expert_loads, lrm_scores, masked_backward,  # noqa: F401
+from .lrm_oracle import (compact, expert_backward, expert_loads, grad_abs_scores, grad_sq_scores,  # noqa: F401
+                         lrm_scores, masked_backward,
                          plan_quotas, pruned_backward, scatter_dx, select, swiglu_backward,
                          unpruned_backward)

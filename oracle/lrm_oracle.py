@@ -92,6 +92,28 @@ def lrm_scores(alpha, g, phi):
 
 
 # ----------------------------------------------------------------------------------------
+# ablation scores  ([EN] "What the measurements show": LRM is compared with selecting by the
+# squared gradient norm, by the absolute gradient magnitude, and with random dropping).
+# Reading: the gradient-only rules look at the upstream gradient g_t of the pair's token alone,
+# so the k pairs of a token score alike ("a gradient-only rule scores them as interchangeable",
+# section "LRM: ..."); "absolute magnitude" is the L1 norm; random dropping selects on caller-
+# drawn uniform numbers with the same top-quota rule.
+# ----------------------------------------------------------------------------------------
+def grad_sq_scores(g, k):
+    """R[t, j] = ||g_t||_2^2 for every choice j of token t.
+    Pinned: equals lrm_scores with alpha = 1 and a unit-norm phi."""
+    gg = np.asarray(g, dtype=np.float64)
+    return np.repeat(np.sum(gg * gg, axis=1)[:, None], k, axis=1)
+
+
+def grad_abs_scores(g, k):
+    """R[t, j] = ||g_t||_1 = sum_h |g_t[h]|.
+    Pinned: on +-c vectors equals ||g||_2^2 / c; equals |g_t[h]| for a one-hot g_t."""
+    gg = np.asarray(g, dtype=np.float64)
+    return np.repeat(np.sum(np.abs(gg), axis=1)[:, None], k, axis=1)
+
+
+# ----------------------------------------------------------------------------------------
 # selection  ([PT]/[ES] "Seleção pela métrica LRM": inside the quota the highest-scoring
 # pairs are kept; [EN] "Three things worth flagging": the guarantee covers an additive
 # local objective, i.e. the kept set maximises the kept score sum per expert)

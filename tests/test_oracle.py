@@ -328,3 +328,34 @@ def test_generator_shapes(name):
     # no expert is chosen twice by one token
     for row in inp["topk_idx"].tolist():
         assert len(set(row)) == wl.k
+
+
+# ------------------------------------------------- ablation score modes ---------------
+def test_grad_sq_is_lrm_with_unit_alpha_and_unit_phi():
+    rng = np.random.default_rng(5)
+    T, k, H, I = 6, 3, 9, 4
+    g = rng.normal(0, 1, (T, H))
+    phi = rng.normal(0, 1, (T, k, I))
+    phi /= np.linalg.norm(phi, axis=2, keepdims=True)
+    assert np.allclose(O.grad_sq_scores(g, k), O.lrm_scores(np.ones((T, k)), g, phi), rtol=1e-12)
+
+
+def test_grad_abs_closed_forms():
+    rng = np.random.default_rng(6)
+    T, k, H, c = 5, 2, 16, 0.37
+    g = c * rng.choice([-1.0, 1.0], size=(T, H))
+    assert np.allclose(O.grad_abs_scores(g, k), O.grad_sq_scores(g, k) / c, rtol=1e-12)
+    onehot = np.zeros((3, H))
+    onehot[np.arange(3), [2, 7, 11]] = [-4.0, 0.5, 3.0]
+    assert np.allclose(O.grad_abs_scores(onehot, 2), [[4.0, 4.0], [0.5, 0.5], [3.0, 3.0]])
+
+
+def test_gradient_only_scores_tie_within_a_token_and_pick_smaller_u():
+    # all k pairs of a token score alike: selection falls back to the pair-index tie-break
+    idx = np.array([[0, 1], [0, 1], [1, 0]])
+    g = np.array([[1.0, 0.0], [2.0, 0.0], [1.0, 1.0]])
+    for fn in (O.grad_sq_scores, O.grad_abs_scores):
+        R = fn(g, 2)
+        seg, kept, _ = O.select(idx, R, np.array([1, 1]), 2)
+        # expert 0 owns pairs 0, 2, 5 with scores R[0,0], R[1,0], R[2,1]; expert 1 owns 1, 3, 4
+        assert kept[0] == [0, 2, 5][int(np.argmax([R[0, 0], R[1, 0], R[2, 1]]))]
