@@ -109,6 +109,25 @@ lrm_status lrm_plan_quotas(const int32_t* topk_idx, int64_t T, int32_t k, int32_
 lrm_status lrm_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H,
                      int32_t I, lrm_dtype dt, float* scores, int32_t* dev_status, cudaStream_t stream);
 
+/* Scores for the selection ablations of "LRMoE: Trimming Backward Work in Memory-Bound MoE
+ * Training", section "What the measurements show". */
+typedef enum lrm_score_kind {
+  LRM_SCORE_LRM = 0,      /* alpha_u^2 * ||g_t||_2^2 * ||phi_u||_2^2 (lrm_score)                  */
+  LRM_SCORE_GRAD_SQ = 1,  /* squared gradient norm ||g_t||_2^2 (every pair of token t alike)     */
+  LRM_SCORE_GRAD_ABS = 2  /* absolute gradient magnitude ||g_t||_1 = sum_h |g_t[h]|              */
+} lrm_score_kind;
+
+/*
+ * Score of every pair under one of the lrm_score_kind rules, fp32 accumulation.  The gradient-
+ * only rules read g alone (alpha and phi may be NULL) and give the k pairs of a token the same
+ * score, so lrm_select falls back to its pair-index tie-break inside a token.  Random dropping,
+ * the pages' third ablation, is lrm_select on caller-drawn uniform scores.  Layouts, errors and
+ * the non-finite flag as for lrm_score.
+ */
+lrm_status lrm_score_mode(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H,
+                          int32_t I, lrm_dtype dt, lrm_score_kind mode, float* scores, int32_t* dev_status,
+                          cudaStream_t stream);
+
 /*
  * Keep each expert's top-quota pairs (Portuguese list, step "Seleção pela métrica LRM": inside
  * the quota the highest-scoring pairs stay).  Expert e keeps min(max(quota_e,0), load_e) pairs:

@@ -14,6 +14,7 @@ STATUS_NAMES = {0: "LRM_OK", 1: "LRM_ERR_INVALID_ARG", 2: "LRM_ERR_SHAPE", 3: "L
 LRM_BF16, LRM_F32 = 0, 1
 LRM_QUOTA_RATIO, LRM_QUOTA_CAP, LRM_QUOTA_EXPLICIT = 0, 1, 2
 LRM_GEMM_DEFAULT, LRM_GEMM_FORCE_SIMT = 0, 1
+LRM_SCORE_LRM, LRM_SCORE_GRAD_SQ, LRM_SCORE_GRAD_ABS = 0, 1, 2
 LRM_MAX_EXPERTS, LRM_MAX_TOPK = 1024, 16
 
 _p, _i32, _i64, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
@@ -30,6 +31,7 @@ SIGNATURES = {
                                        _p, _p, _p, _sz, _i32, _p, _p]),
     "lrm_scatter_dx": (C.c_int, [_p, _p, _i64, _i32, _i32, C.c_int, _p, _p]),
     "lrm_selftest_wait_timeout": (C.c_int, [_p, _i64, _p]),
+    "lrm_score_mode": (C.c_int, [_p, _p, _p, _i64, _i32, _i32, _i32, C.c_int, C.c_int, _p, _p, _p]),
 }
 
 _lib = None

@@ -86,6 +86,18 @@ def lrm_score(alpha, g, phi, scores=None, dev_status=None):
     return scores
 
 
+def lrm_score_mode(alpha, g, phi, mode, scores=None, dev_status=None):
+    """mode: "lrm", "grad_sq" (||g_t||^2) or "grad_abs" (||g_t||_1); phi gives k and I."""
+    T, H = g.shape
+    k, I = phi.shape[-2], phi.shape[-1]
+    modes = {"lrm": L.LRM_SCORE_LRM, "grad_sq": L.LRM_SCORE_GRAD_SQ, "grad_abs": L.LRM_SCORE_GRAD_ABS}
+    scores = torch.empty(T * k, dtype=torch.float32, device=g.device) if scores is None else scores
+    _ok(L.load().lrm_score_mode(_opt(alpha, "alpha", torch.float32), _cuda(g, "g"), _opt(phi, "phi", g.dtype), T, k,
+                                H, I, _dt(g), modes[mode], _cuda(scores, "scores", torch.float32),
+                                _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_score_mode")
+    return scores
+
+
 def lrm_select(topk_idx, scores, quotas, E, cap=None, seg_offsets=None, kept_pair=None, row_of_pair=None,
                ws=None, dev_status=None):
     T, k = topk_idx.shape

@@ -110,6 +110,20 @@ lrm_status lrm_score(const float* alpha, const void* g, const void* phi, int64_t
   return after_launch();
 }
 
+lrm_status lrm_score_mode(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H,
+                          int32_t I, lrm_dtype dt, lrm_score_kind mode, float* scores, int32_t* dev_status,
+                          cudaStream_t stream) {
+  if (mode == LRM_SCORE_LRM) return lrm_score(alpha, g, phi, T, k, H, I, dt, scores, dev_status, stream);
+  if (mode != LRM_SCORE_GRAD_SQ && mode != LRM_SCORE_GRAD_ABS) return LRM_ERR_INVALID_ARG;
+  lrm_status st = check_dims(T, k, 1, H, 8);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (T > 0 && (!g || !scores)) return LRM_ERR_INVALID_ARG;
+  if (!al16(g)) return LRM_ERR_INVALID_ARG;
+  launch_grad_score(g, T, k, H, dt, mode == LRM_SCORE_GRAD_ABS, scores, dev_status, stream);
+  return after_launch();
+}
+
 lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t T, int32_t k,
                       int32_t E, int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair,
                       void* ws, size_t ws_bytes, int32_t* dev_status, cudaStream_t stream) {

@@ -43,6 +43,9 @@ void launch_plan_quotas(const int32_t* topk_idx, int64_t P, int32_t E, int kind,
 void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
                   lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s);
 
+void launch_grad_score(const void* g, int64_t T, int32_t k, int32_t H, lrm_dtype dt, bool abs_mode, float* scores,
+                       int32_t* status, cudaStream_t s);
+
 void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* quotas, int64_t P, int32_t E,
                    int64_t cap, int32_t* seg_offsets, int32_t* kept_pair, int32_t* row_of_pair, const SelectWs& ws,
                    int32_t* status, cudaStream_t s);

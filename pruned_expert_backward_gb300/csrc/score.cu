@@ -5,65 +5,148 @@
 // the down projection's weight gradient, so ||G_u||_F^2 = alpha_u^2 * ||g_t||^2 * ||phi_u||^2
 // and no gradient matrix has to be formed.
 //
-// One warp per pair row; the k warps of a token each reduce g_t (one DRAM read, the rest L2
-// hits) and their own phi_u row.  All loads are 16-byte and coalesced; phi is streamed past L1.
-// No block-wide barrier, so warps retire as soon as their loads return.  HBM-bound.
+// One warp per token: g_t is read once, then the token's k phi rows (contiguous) two rows at a
+// time.  All loads are 16-byte, coalesced and streamed past L1; no block-wide barrier, so warps
+// retire as soon as their loads return.  HBM-bound.
 #include "common.cuh"
 #include "kernels.h"
 
 namespace lrm {
 
+// Per-lane partial sum of squares of one row of nv 16-byte vectors (v = lane, lane+32, ...):
+// all of the lane's loads are issued before any is used (at most MAXV per lane).
+template <typename T, int MAXV>
+__device__ __forceinline__ float lane_sumsq(const T* row, int nv, int lane) {
+  constexpr int VN = VecTraits<T>::N;
+  uint4 buf[MAXV];
+#pragma unroll
+  for (int m = 0; m < MAXV; ++m) {
+    const int v = lane + 32 * m;
+    buf[m] = v < nv ? ld_stream16(row + (int64_t)v * VN) : make_uint4(0, 0, 0, 0);
+  }
+  float acc = 0.f;
+#pragma unroll
+  for (int m = 0; m < MAXV; ++m) {
+    float f[VN];
+    unpack(buf[m], f);
+#pragma unroll
+    for (int q = 0; q < VN; ++q) acc = fmaf(f[q], f[q], acc);
+  }
+  return acc;
+}
+// Same, for rows of any length (a loop; used when a row exceeds MAXV vectors per lane).
 template <typename T>
+__device__ __forceinline__ float lane_sumsq_any(const T* row, int nv, int lane) {
+  constexpr int VN = VecTraits<T>::N;
+  float acc = 0.f;
+  for (int v = lane; v < nv; v += 32) {
+    float f[VN];
+    unpack(ld_stream16(row + (int64_t)v * VN), f);
+#pragma unroll
+    for (int q = 0; q < VN; ++q) acc = fmaf(f[q], f[q], acc);
+  }
+  return acc;
+}
+
+template <typename T, int GV, int PV>
 __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
-                                                   const T* __restrict__ phi, int64_t n_pairs, int k, int H, int I,
+                                                   const T* __restrict__ phi, int64_t n_tok, int k, int H, int I,
                                                    float* __restrict__ scores, int32_t* status) {
-  // One warp per pair row u = (t, j): it reduces phi_u and, on its own, the token's g_t row (the
-  // token's other k-1 warps read g_t too, from L2).  No block-wide barrier: a warp issues all its
-  // loads, reduces, writes its score and retires.
+  // One warp per token: ||g_t||^2 once, then the token's k contiguous phi rows two at a time.
+  // GV / PV bound the 16-byte vectors per lane of a g row / phi row (0 = unbounded, looped).
   constexpr int VN = VecTraits<T>::N;
   const int lane = threadIdx.x & 31;
-  const int64_t u = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
-  if (u >= n_pairs) return;
-  const int64_t t = u / k;
-  const float a = alpha[u];
-  const T* gt = g + t * H;
-  const T* pu = phi + u * (int64_t)I;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= n_tok) return;
   const int nvg = H / VN, nvp = I / VN;
-  float gs = 0.f, ps = 0.f;
-#pragma unroll 4
-  for (int v = lane; v < nvp; v += 32) {
-    float f[VN];
-    unpack(ld_stream16(pu + (int64_t)v * VN), f);
-#pragma unroll
-    for (int q = 0; q < VN; ++q) ps = fmaf(f[q], f[q], ps);
-  }
-#pragma unroll 8
-  for (int v = lane; v < nvg; v += 32) {
-    float f[VN];
-    unpack(ldg16(gt + (int64_t)v * VN), f);
-#pragma unroll
-    for (int q = 0; q < VN; ++q) gs = fmaf(f[q], f[q], gs);
-  }
+  const T* pt = phi + t * k * (int64_t)I;
+  const float my_alpha = lane < k ? alpha[t * k + lane] : 0.f;
+  float gs = GV ? lane_sumsq<T, (GV ? GV : 1)>(g + t * H, nvg, lane) : lane_sumsq_any<T>(g + t * H, nvg, lane);
   gs = warp_sum(gs);
-  ps = warp_sum(ps);
-  if (lane == 0) {
-    const float r = (a * a) * gs * ps;
-    scores[u] = r;
-    if (!isfinite(r)) set_status(status, LRM_ERR_NONFINITE);
+  for (int j = 0; j < k; j += 2) {
+    const bool two = j + 1 < k;
+    const T* r0 = pt + (int64_t)j * I;
+    float p0, p1 = 0.f;
+    if (PV) {
+      p0 = lane_sumsq<T, (PV ? PV : 1)>(r0, nvp, lane);
+      if (two) p1 = lane_sumsq<T, (PV ? PV : 1)>(r0 + I, nvp, lane);
+    } else {
+      p0 = lane_sumsq_any<T>(r0, nvp, lane);
+      if (two) p1 = lane_sumsq_any<T>(r0 + I, nvp, lane);
+    }
+    p0 = warp_sum(p0);
+    p1 = warp_sum(p1);
+    const float a0 = __shfl_sync(0xffffffffu, my_alpha, j);
+    const float a1 = __shfl_sync(0xffffffffu, my_alpha, two ? j + 1 : j);
+    if (lane == 0) {
+      const float s0 = (a0 * a0) * gs * p0;
+      scores[t * k + j] = s0;
+      if (!isfinite(s0)) set_status(status, LRM_ERR_NONFINITE);
+      if (two) {
+        const float s1 = (a1 * a1) * gs * p1;
+        scores[t * k + j + 1] = s1;
+        if (!isfinite(s1)) set_status(status, LRM_ERR_NONFINITE);
+      }
+    }
   }
+}
+
+// Gradient-only ablation scores ("LRMoE: Trimming Backward Work in Memory-Bound MoE Training",
+// section "What the measurements show": squared gradient norm and absolute gradient magnitude):
+// one warp per token computes ||g_t||_2^2 (ABS = false) or ||g_t||_1 (ABS = true) and writes it
+// to the token's k pairs.
+template <typename T, bool ABS>
+__global__ void __launch_bounds__(256) grad_score_kernel(const T* __restrict__ g, int64_t n_tok, int k, int H,
+                                                         float* __restrict__ scores, int32_t* status) {
+  constexpr int VN = VecTraits<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= n_tok) return;
+  const T* gt = g + t * H;
+  float acc = 0.f;
+#pragma unroll 8
+  for (int v = lane; v < H / VN; v += 32) {
+    float f[VN];
+    unpack(ld_stream16(gt + (int64_t)v * VN), f);
+#pragma unroll
+    for (int q = 0; q < VN; ++q) acc = ABS ? acc + fabsf(f[q]) : fmaf(f[q], f[q], acc);
+  }
+  acc = warp_sum(acc);
+  if (lane < k) scores[t * k + lane] = acc;
+  if (lane == 0 && !isfinite(acc)) set_status(status, LRM_ERR_NONFINITE);
+}
+
+void launch_grad_score(const void* g, int64_t T, int32_t k, int32_t H, lrm_dtype dt, bool abs_mode, float* scores,
+                       int32_t* status, cudaStream_t s) {
+  if (T == 0) return;
+  const unsigned blocks = (unsigned)((T + 7) / 8);
+  using B = __nv_bfloat16;
+  if (dt == LRM_BF16 && abs_mode)
+    grad_score_kernel<B, true><<<blocks, 256, 0, s>>>((const B*)g, T, k, H, scores, status);
+  else if (dt == LRM_BF16)
+    grad_score_kernel<B, false><<<blocks, 256, 0, s>>>((const B*)g, T, k, H, scores, status);
+  else if (abs_mode)
+    grad_score_kernel<float, true><<<blocks, 256, 0, s>>>((const float*)g, T, k, H, scores, status);
+  else
+    grad_score_kernel<float, false><<<blocks, 256, 0, s>>>((const float*)g, T, k, H, scores, status);
 }
 
 void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
                   lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s) {
   if (T == 0) return;
-  const int64_t P = T * k;
-  const int64_t blocks = (P + 7) / 8;  // 8 warps (pair rows) per CTA
-  if (dt == LRM_BF16)
-    score_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, s>>>(
-        alpha, (const __nv_bfloat16*)g, (const __nv_bfloat16*)phi, P, k, H, I, scores, status);
-  else
-    score_kernel<float><<<(unsigned)blocks, 256, 0, s>>>(alpha, (const float*)g, (const float*)phi, P, k, H, I,
-                                                         scores, status);
+  const int64_t blocks = (T + 7) / 8;  // 8 warps (tokens) per CTA
+  const int vn = dt == LRM_BF16 ? 8 : 4;
+  const int gv = (H / vn + 31) / 32, pv = (I / vn + 31) / 32;  // vectors per lane of a g / phi row
+  const bool fits = gv <= 16 && pv <= 6;
+#define LRM_SCORE_LAUNCH(TYPE, GV, PV)                                                                 \
+  score_kernel<TYPE, GV, PV><<<(unsigned)blocks, 256, 0, s>>>(alpha, (const TYPE*)g, (const TYPE*)phi, T, k, H, \
+                                                            I, scores, status)
+  if (dt == LRM_BF16) {
+    if (fits) LRM_SCORE_LAUNCH(__nv_bfloat16, 16, 6); else LRM_SCORE_LAUNCH(__nv_bfloat16, 0, 0);
+  } else {
+    if (fits) LRM_SCORE_LAUNCH(float, 16, 6); else LRM_SCORE_LAUNCH(float, 0, 0);
+  }
+#undef LRM_SCORE_LAUNCH
 }
 
 }  // namespace lrm

@@ -249,3 +249,28 @@ def test_host_pipeline_matches_device_path():
     for (dx, seg), j in zip(seen, order):
         assert torch.equal(seg, refs[j][1])
         assert torch.equal(dx, refs[j][0])
+
+
+@pytest.mark.parametrize("mode", ["grad_sq", "grad_abs", "random"])
+def test_ablation_scores_and_selection(mode):
+    """The pages' selection ablations: gradient-only scores (fp64 parity 1e-5) and random
+    dropping (caller-drawn uniform scores); selection on them is bit-exact with the oracle's."""
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.small_workload("ablate", 1500, 512, 256, 32, 8)
+    inp = W.generate(wl, "cuda", seed=7)
+    _, q = lrm.lrm_plan_quotas(inp["topk_idx"], wl.E, "ratio", 8, 10)
+    if mode == "random":
+        gen = torch.Generator(device="cuda").manual_seed(11)
+        scores = torch.rand(wl.P, generator=gen, device="cuda")
+    else:
+        scores = lrm.lrm_score_mode(None, inp["g"], inp["phi"], mode)
+        fn = oracle.grad_sq_scores if mode == "grad_sq" else oracle.grad_abs_scores
+        want = fn(to_np(inp["g"]), wl.k).reshape(-1)
+        got = scores.cpu().double().numpy()
+        assert np.max(np.abs(got - want) / want) <= 1e-5
+    seg, kept, rop = lrm.lrm_select(inp["topk_idx"], scores, q, wl.E)
+    torch.cuda.synchronize()
+    oseg, okept, orop = oracle.select(to_np(inp["topk_idx"]), scores.cpu().numpy(), to_np(q), wl.E)
+    assert np.array_equal(to_np(seg), oseg)
+    assert np.array_equal(to_np(kept)[: int(oseg[-1])], okept)
+    assert np.array_equal(to_np(rop), orop)
