@@ -4,5 +4,5 @@ Only tests/, __graft_entry__.smoke() and bench.py's CPU-baseline / reference arm
 """
 from .lrm_oracle import (compact, expert_backward, expert_loads, grad_abs_scores, grad_sq_scores,  # noqa: F401
                          lrm_scores, masked_backward,
-                         plan_quotas, pruned_backward, scatter_dx, select, swiglu_backward,
+                         plan_quotas, pruned_backward, router_grad, scatter_dx, select, swiglu_backward,
                          unpruned_backward)

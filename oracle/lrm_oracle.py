@@ -32,6 +32,8 @@ Readings where the pages are silent (each also listed in the design doc):
     easy to get wrong"; [PT] step "Compactação física").
   * Ties in score are broken by pair index u ascending; inside a segment the compacted
     rows are in u ascending order.
+  * The routing-weight gradient dL/dalpha_u = g_t . (W_down[e] phi_u) is computed for the
+    retained pairs only; a dropped pair's is 0 (same reading as the one above).
   * Quotas are integers; ratio rule quota = ceil(num/den * load) in exact integer math,
     cap rule quota = min(load, cap); an explicit quota above the load keeps the whole load.
 
@@ -240,6 +242,37 @@ def scatter_dx(row_of_pair, dX_c, T, k):
         m = rows >= 0
         dX[m] += dX_c[rows[m]]
     return dX
+
+
+# ----------------------------------------------------------------------------------------
+# router gradient  (the layer output is out_t = sum_j alpha_{t,j} y_{t,j} with the expert
+# output y_{t,j} = W_down[e] phi_{t,j}, so the loss gradient with respect to a routing weight
+# is dL/dalpha_{t,j} = g_t . y_{t,j}.  The pages say nothing about it under pruning.  Reading:
+# a dropped pair is removed from the whole expert backward, so its routing-weight gradient is
+# 0 as well; a retained pair's is the exact one.)
+# ----------------------------------------------------------------------------------------
+def router_grad(row_of_pair, topk_idx, g, phi, w_down, pairs=None):
+    """dalpha[u] = g_t . (W_down[e_u] phi_u) for a retained pair u = t*k + j (row_of_pair[u] >= 0),
+    0 for a dropped one; returned flat, [T*k].  `pairs` limits the work to those pair indices
+    (the rest stay 0), for sampled checks at large sizes.
+    Pinned: with quota = load it equals torch fp64 autograd's dL/dalpha of the explicit forward;
+    on a pruned selection it equals (dPhi_u . phi_u) / alpha_u with dPhi taken from the
+    zero-masked full-shape rows."""
+    idx = np.asarray(topk_idx).reshape(-1)
+    rop = np.asarray(row_of_pair).reshape(-1)
+    T = np.asarray(g).shape[0]
+    k = idx.size // T if T > 0 else 1
+    G = np.asarray(g, dtype=np.float64)
+    Phi = np.asarray(phi, dtype=np.float64).reshape(idx.size, -1)
+    Wd = np.asarray(w_down, dtype=np.float64)
+    out = np.zeros(idx.size)
+    todo = range(idx.size) if pairs is None else (int(u) for u in pairs)
+    for u in todo:
+        if rop[u] < 0:
+            continue
+        y = Wd[int(idx[u])] @ Phi[u]          # the expert's output for this pair (H)
+        out[u] = float(G[u // k] @ y)
+    return out
 
 
 # ----------------------------------------------------------------------------------------

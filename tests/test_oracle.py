@@ -78,7 +78,7 @@ def explicit_forward_grads(inp):
     x = torch.tensor(inp["x"], dtype=torch.float64, requires_grad=True)
     Wgu = torch.tensor(inp["w_gate_up"], dtype=torch.float64, requires_grad=True)
     Wd = torch.tensor(inp["w_down"], dtype=torch.float64, requires_grad=True)
-    alpha = torch.tensor(inp["alpha"], dtype=torch.float64)
+    alpha = torch.tensor(inp["alpha"], dtype=torch.float64, requires_grad=True)
     g = torch.tensor(inp["g"], dtype=torch.float64)
     idx = inp["topk_idx"]
     T, k = idx.shape
@@ -93,7 +93,7 @@ def explicit_forward_grads(inp):
             out = out + alpha[t, j] * (Wd[e] @ act)
         loss = loss + torch.dot(g[t], out)
     loss.backward()
-    return Wgu.grad.numpy(), Wd.grad.numpy(), x.grad.numpy()
+    return Wgu.grad.numpy(), Wd.grad.numpy(), x.grad.numpy(), alpha.grad.numpy()
 
 
 def fp64_consistent_inputs(seed=0, T=11, H=6, I=5, E=4, k=2):
@@ -128,8 +128,41 @@ def rel(a, b):
 def autograd_pin_error(seed=0):
     inp = fp64_consistent_inputs(seed)
     out = O.unpruned_backward(inp)
-    gWgu, gWd, gx = explicit_forward_grads(inp)
+    gWgu, gWd, gx, _ = explicit_forward_grads(inp)
     return max(rel(out["dw_gate_up"], gWgu), rel(out["dw_down"], gWd), rel(out["dx"], gx))
+
+
+def router_autograd_pin_error(seed=0):
+    """quota = load: the oracle's dalpha against torch fp64 autograd's dL/dalpha."""
+    inp = fp64_consistent_inputs(seed)
+    out = O.unpruned_backward(inp)
+    dalpha = O.router_grad(out["row_of_pair"], inp["topk_idx"], inp["g"], inp["phi"], inp["w_down"])
+    *_, galpha = explicit_forward_grads(inp)
+    return rel(dalpha, galpha.reshape(-1))
+
+
+def router_masked_pin_error(seed=0):
+    """Pruned selection: dalpha against the zero-masked full-shape route, where every pair's
+    dPhi_u = (mask_u alpha_u g_t) W_down[e] and dalpha_u = (dPhi_u . phi_u) / alpha_u.
+    Returns (relative error, number of dropped pairs)."""
+    inp = fp64_consistent_inputs(seed, T=13, E=3, k=2)
+    idx = inp["topk_idx"]
+    E = inp["w_down"].shape[0]
+    _, quotas = O.plan_quotas(idx, E, "ratio", 1, 2)
+    out = O.pruned_backward(inp, quotas)
+    rop = out["row_of_pair"].reshape(-1)
+    dalpha = O.router_grad(rop, idx, inp["g"], inp["phi"], inp["w_down"])
+    T, k = idx.shape
+    alt = np.zeros(T * k)
+    for t in range(T):
+        for j in range(k):
+            u = t * k + j
+            a = inp["alpha"][t, j]
+            dy = (a if rop[u] >= 0 else 0.0) * inp["g"][t]
+            dphi = dy @ inp["w_down"][idx[t, j]]
+            alt[u] = float(dphi @ inp["phi"][t, j]) / a
+    assert np.all(dalpha[rop < 0] == 0.0)
+    return rel(dalpha, alt), int(np.sum(rop < 0))
 
 
 def swiglu_fd_error(seed=0):
@@ -213,6 +246,17 @@ def test_swiglu_derivative_finite_differences():
 def test_full_quota_reduces_to_autograd_backward():
     for seed in range(3):
         assert autograd_pin_error(seed) < 1e-12
+
+
+def test_router_grad_full_quota_equals_autograd():
+    for seed in range(3):
+        assert router_autograd_pin_error(seed) < 1e-12
+
+
+def test_router_grad_pruned_equals_masked_route():
+    err, n_dropped = router_masked_pin_error()
+    assert n_dropped > 0
+    assert err < 1e-12
 
 
 def test_compacted_equals_zero_masked_full_shape():
@@ -315,6 +359,32 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     with monkeypatch.context() as m:
         m.setattr(O, "scatter_dx", _planted_scatter_drops_last_choice)
         assert autograd_pin_error() > 1e-3
+    real_router = O.router_grad
+
+    def router_scaled_by_alpha(rop, idx, g, phi, w_down, pairs=None):
+        # returns alpha_u * g_t . y_u (the gradient of the alpha-scaled output row)
+        T, k = np.asarray(idx).shape
+        a = fp64_consistent_inputs(0)["alpha"].reshape(-1)
+        return real_router(rop, idx, g, phi, w_down, pairs) * (a if a.size == T * k else 1.0)
+
+    def router_ignores_selection(rop, idx, g, phi, w_down, pairs=None):
+        return real_router(np.zeros_like(np.asarray(rop)), idx, g, phi, w_down, pairs)
+
+    def router_first_choice_expert(rop, idx, g, phi, w_down, pairs=None):
+        idx = np.asarray(idx).copy()
+        idx[:, 1:] = idx[:, :1]
+        return real_router(rop, idx, g, phi, w_down, pairs)
+
+    with monkeypatch.context() as m:
+        m.setattr(O, "router_grad", router_scaled_by_alpha)
+        assert router_autograd_pin_error() > 1e-3
+    with monkeypatch.context() as m:
+        m.setattr(O, "router_grad", router_first_choice_expert)
+        assert router_autograd_pin_error() > 1e-3
+    with monkeypatch.context() as m:
+        m.setattr(O, "router_grad", router_ignores_selection)
+        with pytest.raises(AssertionError):
+            router_masked_pin_error()
 
 
 @pytest.mark.parametrize("name", ["tiny_f32", "load_example"])
