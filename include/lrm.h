@@ -177,6 +177,13 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
  * An expert with R_e = 0 gets dw = 0 exactly.  w_gate_up [E,2I,H] (gate rows first),
  * w_down [E,H,I].  Accumulation is fp32.  `flags` is LRM_GEMM_DEFAULT or LRM_GEMM_FORCE_SIMT.
  * seg_offsets must be non-decreasing with seg_offsets[E] <= cap (as lrm_select writes them).
+ * Optional row_dot [cap] fp32 (NULL skips it; 4-byte aligned): for every retained row
+ * r < seg_offsets[E], row_dot[r] = sum_i dphi[r,i] * phi~[r,i], where phi~ = SiLU(gate)*up is
+ * recomputed in fp32 from h_c inside the same epilogue; for the pair u = (t, e) of row r that is
+ * alpha_u * (g_t . W_down[e] phi_u), the input of lrm_router_grad.  Its parts are summed in a
+ * fixed order (deterministic).  Rows >= seg_offsets[E] are not written.
+ * ws, ws_bytes: scratch of at least lrm_workspace_size bytes (with row_dot it must cover `cap`
+ * rows: lrm_workspace_size for T*k >= cap does).
  * Errors: host as usual; LRM_ERR_UNSUPPORTED when the tensor-core kernels are requested on a
  * device that is not sm_103; device LRM_ERR_TIMEOUT if a pipeline wait gives up (the kernel
  * then returns early and its outputs are incomplete).
@@ -184,8 +191,24 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
 lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
                                 const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E,
                                 int32_t H, int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up,
-                                float* dw_down, void* dh_c, void* dx_c, void* ws, size_t ws_bytes,
-                                int32_t flags, int32_t* dev_status, cudaStream_t stream);
+                                float* dw_down, void* dh_c, void* dx_c, float* row_dot, void* ws,
+                                size_t ws_bytes, int32_t flags, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Routing-weight gradient of the pairs.  The layer output is out_t = sum_j alpha_{t,j} y_{t,j}
+ * with y_u = W_down[e_u] phi_u (the expert output), so dL/dalpha_u = g_t . y_u.  The LRMoE
+ * pages say nothing about it under pruning; here a dropped pair, removed from the whole expert
+ * backward ("The part that is easy to get wrong": only retained rows are packed and computed),
+ * gets 0, and a retained pair the exact value:
+ *   r = row_of_pair[u];  dalpha[u] = (0 <= r < cap) ? row_dot[r] / alpha_u : 0
+ * with row_dot from lrm_grouped_backward.  Where alpha_u == 0 the alpha-scaled rows carry no
+ * trace of g_t . y_u and dalpha[u] = 0.
+ *   row_of_pair [T*k] int32, alpha [T*k] fp32, row_dot [cap] fp32  ->  dalpha [T*k] fp32.
+ * Errors: LRM_ERR_INVALID_ARG (NULL pointer, cap outside [0, INT32_MAX]), LRM_ERR_SHAPE,
+ * LRM_ERR_CUDA.
+ */
+lrm_status lrm_router_grad(const int32_t* row_of_pair, const float* alpha, const float* row_dot, int64_t T,
+                           int32_t k, int64_t cap, float* dalpha, cudaStream_t stream);
 
 /*
  * Back to the original token layout (Portuguese list: "the result returns to the original

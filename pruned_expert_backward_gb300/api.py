@@ -134,7 +134,9 @@ def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=
 
 
 def lrm_grouped_backward(seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, cap, dw_gate_up=None,
-                         dw_down=None, dh_c=None, dx_c=None, ws=None, flags=L.LRM_GEMM_DEFAULT, dev_status=None):
+                         dw_down=None, dh_c=None, dx_c=None, ws=None, flags=L.LRM_GEMM_DEFAULT, dev_status=None,
+                         row_dot=None):
+    """row_dot: optional fp32 [cap] output (dphi . phi of each retained row, for lrm_router_grad)."""
     E, H, I = w_down.shape
     dev, dt = w_down.device, w_down.dtype
     rows = max(int(cap), 1)
@@ -143,15 +145,26 @@ def lrm_grouped_backward(seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, 
     dh_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if dh_c is None else dh_c
     dx_c = torch.empty(rows, H, dtype=dt, device=dev) if dx_c is None else dx_c
     if ws is None:
-        ws = torch.empty(lrm_workspace_size(0, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
+        ws_rows = int(cap) if row_dot is not None else 0
+        ws = torch.empty(lrm_workspace_size(ws_rows, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
     _ok(L.load().lrm_grouped_backward(
         _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(dy_c, "dy_c", dt), _cuda(x_c, "x_c", dt),
         _cuda(h_c, "h_c", dt), _cuda(phi_c, "phi_c", dt), _cuda(w_gate_up, "w_gate_up", dt),
         _cuda(w_down, "w_down", dt), E, H, I, _dt(w_down), int(cap),
         _cuda(dw_gate_up, "dw_gate_up", torch.float32), _cuda(dw_down, "dw_down", torch.float32),
-        _cuda(dh_c, "dh_c", dt), _cuda(dx_c, "dx_c", dt), _cuda(ws, "ws"), ws.numel(), int(flags),
+        _cuda(dh_c, "dh_c", dt), _cuda(dx_c, "dx_c", dt), _opt(row_dot, "row_dot", torch.float32),
+        _cuda(ws, "ws"), ws.numel(), int(flags),
         _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_grouped_backward")
     return dw_gate_up, dw_down, dh_c, dx_c
+
+
+def lrm_router_grad(row_of_pair, alpha, row_dot, T, k, cap, dalpha=None):
+    """dL/dalpha [T*k] fp32 of the retained pairs (0 for dropped ones) from lrm_grouped_backward's row_dot."""
+    dalpha = torch.empty(T * k, dtype=torch.float32, device=alpha.device) if dalpha is None else dalpha
+    _ok(L.load().lrm_router_grad(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(alpha, "alpha", torch.float32),
+                                 _opt(row_dot, "row_dot", torch.float32), T, k, int(cap),
+                                 _cuda(dalpha, "dalpha", torch.float32), _stream()), "lrm_router_grad")
+    return dalpha
 
 
 def lrm_scatter_dx(row_of_pair, dx_c, T, k, dx=None):
@@ -168,11 +181,13 @@ class PrunedBackward:
     grouped backward -> scatter on the current stream; no host synchronisation.
 
     cap defaults to T*k, which can never overflow; a caller that knows sum(min(quota, load))
-    may pass it to shrink the compacted buffers."""
+    may pass it to shrink the compacted buffers.  router_grad=True also produces dL/dalpha of
+    every pair (`dalpha`, fp32 [T*k]; 0 for dropped pairs)."""
 
-    def __init__(self, T, k, E, H, I, dtype=torch.bfloat16, device="cuda", cap=None, flags=L.LRM_GEMM_DEFAULT):
+    def __init__(self, T, k, E, H, I, dtype=torch.bfloat16, device="cuda", cap=None, flags=L.LRM_GEMM_DEFAULT,
+                 router_grad=False):
         self.T, self.k, self.E, self.H, self.I = T, k, E, H, I
-        self.dtype, self.flags = dtype, flags
+        self.dtype, self.flags, self.router_grad = dtype, flags, router_grad
         self.cap = T * k if cap is None else int(cap)
         dev = torch.device(device)
         rows = max(self.cap, 1)
@@ -192,6 +207,8 @@ class PrunedBackward:
         self.dx = torch.empty(T, H, dtype=dtype, device=dev)
         self.ws = torch.empty(lrm_workspace_size(T, k, E, H, I, dtype), dtype=torch.uint8, device=dev)
         self.dev_status = torch.zeros(1, **i32)
+        self.row_dot = torch.empty(rows, dtype=torch.float32, device=dev) if router_grad else None
+        self.dalpha = torch.empty(max(T * k, 1), dtype=torch.float32, device=dev) if router_grad else None
 
     def run(self, inp, quotas):
         """inp: dict with topk_idx [T,k] int32, alpha [T,k] fp32, x, g [T,H], h [T,k,2I], phi [T,k,I],
@@ -204,15 +221,19 @@ class PrunedBackward:
         lrm_grouped_backward(self.seg_offsets, self.dy_c, self.x_c, self.h_c, self.phi_c, inp["w_gate_up"],
                              inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
                              dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
-                             dev_status=self.dev_status)
+                             dev_status=self.dev_status, row_dot=self.row_dot)
         lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx)
+        if self.router_grad:
+            lrm_router_grad(self.row_of_pair, inp["alpha"], self.row_dot, self.T, self.k, self.cap,
+                            dalpha=self.dalpha)
         return self
 
     def outputs(self):
         return {"scores": self.scores, "seg_offsets": self.seg_offsets, "kept_pair": self.kept_pair,
                 "row_of_pair": self.row_of_pair, "dy_c": self.dy_c, "x_c": self.x_c, "h_c": self.h_c,
                 "phi_c": self.phi_c, "dh_c": self.dh_c, "dx_c": self.dx_c, "dw_gate_up": self.dw_gate_up,
-                "dw_down": self.dw_down, "dx": self.dx, "dev_status": self.dev_status}
+                "dw_down": self.dw_down, "dx": self.dx, "dev_status": self.dev_status,
+                "row_dot": self.row_dot, "dalpha": self.dalpha}
 
 
 class HostPipeline:

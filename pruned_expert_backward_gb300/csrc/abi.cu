@@ -33,6 +33,14 @@ lrm_status after_launch() {
 
 size_t gemm_ws_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 1)) + 128 * 4 * (size_t)E; }
 
+// lrm_grouped_backward's scratch: tile tables and tensor maps, then (only when row_dot is
+// requested) the dphi . phi parts of every row.
+size_t grouped_ws_bytes(int64_t cap, int32_t E, int32_t I, bool row_dot) {
+  size_t b = up(gemm_ws_bytes(E));
+  if (row_dot) b += up(sizeof(float) * (size_t)(cap > 0 ? cap : 1) * dot_parts_max(I));
+  return b;
+}
+
 WsLayout workspace_layout(int64_t P, int32_t E) {
   WsLayout w{};
   const int64_t nc = (P + kSelChunk - 1) / kSelChunk;
@@ -76,7 +84,8 @@ lrm_status lrm_workspace_size(int64_t T, int32_t k, int32_t E, int32_t H, int32_
   lrm_status st = check_dims(T, k, E, H, I);
   if (st) return st;
   if ((st = check_dt(dt))) return st;
-  *bytes = workspace_layout(T * k, E).total;
+  const size_t sel = workspace_layout(T * k, E).total, grp = grouped_ws_bytes(T * k, E, I, true);
+  *bytes = sel > grp ? sel : grp;
   return LRM_OK;
 }
 
@@ -168,8 +177,8 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
 lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
                                 const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E, int32_t H,
                                 int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
-                                void* dx_c, void* ws, size_t ws_bytes, int32_t flags, int32_t* dev_status,
-                                cudaStream_t stream) {
+                                void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
+                                int32_t* dev_status, cudaStream_t stream) {
   lrm_status st = check_dims(0, 1, E, H, I);
   if (st) return st;
   if ((st = check_dt(dt))) return st;
@@ -180,12 +189,13 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
   const void* ptrs[] = {dy_c, x_c, h_c, phi_c, w_gate_up, w_down, dw_gate_up, dw_down, dh_c, dx_c};
   for (const void* p : ptrs)
     if (!al16(p)) return LRM_ERR_INVALID_ARG;
-  if (!ws) return LRM_ERR_WORKSPACE;
+  if (row_dot && (reinterpret_cast<uintptr_t>(row_dot) & 3u)) return LRM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < grouped_ws_bytes(cap, E, I, row_dot != nullptr)) return LRM_ERR_WORKSPACE;
+  float* dot_part = row_dot ? reinterpret_cast<float*>(static_cast<char*>(ws) + up(gemm_ws_bytes(E))) : nullptr;
   GroupedArgs a{seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, E, H, I, cap,
-                dw_gate_up, dw_down, dh_c, dx_c, dev_status};
+                dw_gate_up, dw_down, dh_c, dx_c, dev_status, row_dot, dot_part};
   if (dt == LRM_BF16 && flags == LRM_GEMM_DEFAULT) {
     // workspace: tile tables and per-expert tensor maps at the start of ws
-    if (ws_bytes < gemm_ws_bytes(E)) return LRM_ERR_WORKSPACE;
     GemmWs gw;
     gw.plan = static_cast<int32_t*>(ws);
     gw.maps = static_cast<char*>(ws) + up(sizeof(int32_t) * (2 * (size_t)E + 1));
@@ -203,6 +213,17 @@ lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t 
   if (T > 0 && (!row_of_pair || !dx_c || !dx)) return LRM_ERR_INVALID_ARG;
   if (!al16(dx_c) || !al16(dx)) return LRM_ERR_INVALID_ARG;
   launch_scatter_dx(row_of_pair, dx_c, T, k, H, dt, dx, stream);
+  return after_launch();
+}
+
+lrm_status lrm_router_grad(const int32_t* row_of_pair, const float* alpha, const float* row_dot, int64_t T,
+                           int32_t k, int64_t cap, float* dalpha, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, 1, 8, 8);
+  if (st) return st;
+  if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
+  if (T > 0 && (!row_of_pair || !alpha || !dalpha)) return LRM_ERR_INVALID_ARG;
+  if (T > 0 && cap > 0 && !row_dot) return LRM_ERR_INVALID_ARG;
+  launch_router_grad(row_of_pair, alpha, row_dot, T * k, cap, dalpha, stream);
   return after_launch();
 }
 

@@ -58,7 +58,8 @@ __device__ void mtile_prefix(const int32_t* seg, int E, int* s_prefix) {
 template <typename T, int EPI>
 __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ seg, int E,
                                                   const T* __restrict__ A, const T* __restrict__ B, int K, int N,
-                                                  const T* __restrict__ h_c, T* __restrict__ out) {
+                                                  const T* __restrict__ h_c, T* __restrict__ out,
+                                                  float* __restrict__ dot_part, int n_part) {
   __shared__ int s_prefix[LRM_MAX_EXPERTS + 1];
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
     }
     __syncthreads();
   }
+  float rdot[4] = {0.f, 0.f, 0.f, 0.f};  // EPI_SWIGLU: dphi . phi over this thread's columns
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = r0 + ty * 4 + i;
@@ -118,11 +120,23 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
         const float up = to_f(h_c[(int64_t)r * 2 * N + N + n]);
         const float sg = 1.f / (1.f + expf(-gate));
         const float dphi = acc[i][j];
+        const float du = dphi * gate * sg;
         out[(int64_t)r * 2 * N + n] = from_f<T>(dphi * up * sg * (1.f + gate * (1.f - sg)));
-        out[(int64_t)r * 2 * N + N + n] = from_f<T>(dphi * gate * sg);
+        out[(int64_t)r * 2 * N + N + n] = from_f<T>(du);
+        rdot[i] = fmaf(du, up, rdot[i]);  // dphi * phi, phi = gate * s * up
       } else {
         out[(int64_t)r * N + n] = from_f<T>(acc[i][j]);
       }
+    }
+  }
+  if (EPI == EPI_SWIGLU && dot_part != nullptr) {
+    // the 16 threads of a row group (tx = lane & 15) add their parts in a fixed order
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+#pragma unroll
+      for (int o = 1; o < 16; o <<= 1) rdot[i] += __shfl_xor_sync(0xffffffffu, rdot[i], o);
+      const int r = r0 + ty * 4 + i;
+      if (tx == 0 && r < r1) dot_part[(int64_t)r * n_part + blockIdx.y] = rdot[i];
     }
   }
 }
@@ -190,8 +204,10 @@ void run_all(const GroupedArgs& a, cudaStream_t s) {
   T* dx = (T*)a.dx_c;
   if (mtiles > 0) {
     // dphi + SwiGLU backward: [R_e, H] x [H, I]
-    varm_kernel<T, EPI_SWIGLU><<<dim3((unsigned)mtiles, (I + BN - 1) / BN), NT, 0, s>>>(
-        a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh);
+    const int n_part = (I + BN - 1) / BN;
+    varm_kernel<T, EPI_SWIGLU><<<dim3((unsigned)mtiles, n_part), NT, 0, s>>>(
+        a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh, a.row_dot ? a.dot_part : nullptr, n_part);
+    if (a.row_dot != nullptr) launch_row_dot(a.dot_part, n_part, a.seg_offsets, E, a.cap, a.row_dot, s);
   }
   // dW_down[e] = dy_c^T phi_c : [H, I]
   vark_kernel<T><<<dim3((I + BN - 1) / BN, (H + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, dy, pc, H, I,
@@ -202,7 +218,7 @@ void run_all(const GroupedArgs& a, cudaStream_t s) {
   if (mtiles > 0) {
     // dx_c = dh_c W_gate_up[e] : [R_e, 2I] x [2I, H]
     varm_kernel<T, EPI_STORE><<<dim3((unsigned)mtiles, (H + BN - 1) / BN), NT, 0, s>>>(
-        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx);
+        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx, nullptr, 0);
   }
 }
 

@@ -80,6 +80,8 @@ struct TcParams {
   int32_t* status;
   const CUtensorMap* maps_a;  // VK: per-expert maps of A and B whose row extent ends at the
   const CUtensorMap* maps_b;  //     expert's segment end (TMA zero-fills the rows beyond it)
+  float* dot_part;            // VM_SWIGLU, optional: [rows][n_part] parts of dphi . phi (one per
+  int n_part;                 //     128 output columns), summed in order by the reduce kernel
 };
 
 // ---------------------------------------------------------------- PTX wrappers -------
@@ -431,6 +433,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // (tcgen05.ld 32x32b), staged in shared memory and written back row-contiguous, so global
     // stores (and the SwiGLU h_c loads) are coalesced; var-M rows are masked at the segment end.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+    const int sub = lane >> 2, piece = lane & 3;  // var-M stores: lane owns 8 columns of one row
     float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : kEpiBytes));
     int lt = 0;
     for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
@@ -443,6 +446,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int row_base = p.kind == VK ? d.m0 + q * 32 : d.row0 + q * 32;
       const int row_lim = p.kind == VK ? p.M : d.row_end;
       const int nrows = d.has_rows ? min(32, row_lim - row_base) : 0;
+      // VM_SWIGLU: this lane's part of dphi . phi for rows i*8 + sub over its columns, where
+      // dphi . phi = sum of dup * up (dup = dphi * gate * s, phi = gate * s * up)
+      float rdot[4] = {0.f, 0.f, 0.f, 0.f};
       for (int c = half * 4; c < half * 4 + 4 && nrows > 0; ++c) {
         const int n = d.n0 + c * 32;
         if (n >= p.N) break;  // warp-uniform
@@ -472,7 +478,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncwarp();
         {
           // bf16 rows: 8 rows x 64 B per instruction; lane owns 8 columns of one row
-          const int sub = lane >> 2, piece = lane & 3;
           const int col = n + piece * 8;
           if (p.kind == VM_SWIGLU) {
             const int I = p.N;
@@ -500,6 +505,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                   const float sg = 1.f / (1.f + __expf(-gate[j]));
                   dg[j] = dphi * up[j] * sg * (1.f + gate[j] * (1.f - sg));
                   du[j] = dphi * gate[j] * sg;
+                  rdot[i] = fmaf(du[j], up[j], rdot[i]);
                 }
                 __nv_bfloat16* orow = reinterpret_cast<__nv_bfloat16*>(p.out) + (int64_t)(row_base + rr) * 2 * I;
                 st16(orow + col, pack(dg));
@@ -522,6 +528,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
         __syncwarp();
+      }
+      if (p.kind == VM_SWIGLU && p.dot_part != nullptr && nrows > 0 && d.n0 + half * 128 < p.N) {
+        // warp-uniform; the four lanes of a row add their parts in a fixed order
+        const int part = d.n0 / 128 + half;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          rdot[i] += __shfl_xor_sync(0xffffffffu, rdot[i], 1);
+          rdot[i] += __shfl_xor_sync(0xffffffffu, rdot[i], 2);
+          const int rr = i * 8 + sub;
+          if (piece == 0 && rr < nrows) p.dot_part[(int64_t)(row_base + rr) * p.n_part + part] = rdot[i];
+        }
       }
       tc_fence_before();
       __syncwarp();
@@ -748,8 +765,9 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   // dphi = dy_c W_down[e], SwiGLU backward fused -> dh_c
   if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !make_map_3d(&mB, g.w_down, E, H, I)) return LRM_ERR_CUDA;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
-             (const __nv_bfloat16*)g.h_c, g.status, nullptr, nullptr};
+             (const __nv_bfloat16*)g.h_c, g.status, nullptr, nullptr, g.dot_part, (I + 127) / 128};
   if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
+  if (g.row_dot != nullptr) launch_row_dot(g.dot_part, p.n_part, g.seg_offsets, E, g.cap, g.row_dot, s);
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
                nullptr, g.status, maps + 0 * E, maps + 1 * E};

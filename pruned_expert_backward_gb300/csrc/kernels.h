@@ -65,7 +65,17 @@ struct GroupedArgs {
   float *dw_gate_up, *dw_down;
   void *dh_c, *dx_c;
   int32_t* status;
+  float* row_dot;   // optional [cap]: dphi . phi per retained row
+  float* dot_part;  // scratch for row_dot: [cap][dot_parts_max(I)]
 };
+
+// Parts of the dphi . phi row sums: one per 128 output columns (tensor-core path) or per 64
+// (CUDA-core path); scratch is sized for the larger count.
+inline int dot_parts_max(int32_t I) { return (I + 63) / 64; }
+void launch_row_dot(const float* part, int n_part, const int32_t* seg_offsets, int32_t E, int64_t cap,
+                    float* row_dot, cudaStream_t s);
+void launch_router_grad(const int32_t* row_of_pair, const float* alpha, const float* row_dot, int64_t P,
+                        int64_t cap, float* dalpha, cudaStream_t s);
 
 void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s);
 // Returns LRM_OK, or LRM_ERR_UNSUPPORTED / LRM_ERR_CUDA when the tensor-core path cannot run.

@@ -41,14 +41,14 @@ def gpu_quotas(inp, wl):
     return lrm.lrm_plan_quotas(inp["topk_idx"], wl.E, kind, num, den, cap, explicit=ex)
 
 
-def run_cuda_path(wl, seed=0, flags=0, quotas=None, cap=None, device="cuda"):
+def run_cuda_path(wl, seed=0, flags=0, quotas=None, cap=None, device="cuda", router_grad=False):
     import pruned_expert_backward_gb300 as lrm
     inp = W.generate(wl, device, seed=seed)
     loads, q = gpu_quotas(inp, wl)
     if quotas is not None:
         q = torch.as_tensor(np.asarray(quotas), dtype=torch.int32, device=device)
     pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, device=device, cap=cap,
-                            flags=flags)
+                            flags=flags, router_grad=router_grad)
     pb.run(inp, q)
     torch.cuda.synchronize()
     return inp, loads, q, pb

@@ -52,7 +52,16 @@ def test_workspace_size_and_host_validation():
     # unknown GEMM flag
     fake = C.c_void_p(0x1000)
     assert lib.lrm_grouped_backward(fake, fake, fake, fake, fake, fake, fake, 4, 64, 32, 0, 16, fake, fake, fake,
-                                    fake, fake, 1 << 20, 5, None, None) == 1
+                                    fake, None, fake, 1 << 20, 5, None, None) == 1
+    # row_dot needs room for the dphi . phi parts of every row in the workspace
+    small = C.c_size_t(0)
+    assert lib.lrm_workspace_size(0, 1, 4, 64, 32, 0, C.byref(small)) == 0
+    assert lib.lrm_grouped_backward(fake, fake, fake, fake, fake, fake, fake, 4, 64, 32, 0, 1 << 20, fake, fake,
+                                    fake, fake, fake, fake, small.value, 0, None, None) == 4
+    # router gradient: null pointers, negative cap
+    assert lib.lrm_router_grad(None, fake, fake, 16, 2, 32, fake, None) == 1
+    assert lib.lrm_router_grad(fake, fake, None, 16, 2, 32, fake, None) == 1
+    assert lib.lrm_router_grad(fake, fake, fake, 16, 2, -1, fake, None) == 1
     # workspace too small for select
     assert lib.lrm_select(fake, fake, fake, 16, 2, 4, 32, fake, fake, fake, fake, 8, None, None) == 4
     # misaligned pointer

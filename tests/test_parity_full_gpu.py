@@ -125,3 +125,35 @@ def test_full_size_parity(name):
     want = oracle.scatter_dx(sub_rop, dXc, T, k)[toks]
     got = _np(pb.dx.index_select(0, torch.as_tensor(toks, device="cuda"))).astype(np.float64)
     assert rel_fro(got, want) <= tol, (name, "dx", rel_fro(got, want))
+
+
+@pytest.mark.parametrize("name", ["qwen3_t8k_d20", "glm45_t32k_d20"])
+def test_full_size_router_grad(name):
+    """dL/dalpha at full size: exact zeros for every dropped pair, sampled retained pairs against
+    the oracle (one expert's weights at a time)."""
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.WORKLOADS[name]
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    inp = W.generate(wl, "cuda", seed=0)
+    _, q = gpu_quotas(inp, wl)
+    pb = lrm.PrunedBackward(T, k, E, H, I, dtype=wl.torch_dtype, router_grad=True)
+    pb.run(inp, q)
+    torch.cuda.synchronize()
+    assert int(pb.dev_status.item()) == 0
+    rop = to_np(pb.row_of_pair)
+    dalpha = pb.dalpha.cpu().numpy().astype(np.float64)
+    assert np.all(dalpha[rop < 0] == 0)
+    rng = np.random.default_rng(1)
+    kept = np.nonzero(rop >= 0)[0]
+    pairs = np.sort(rng.choice(kept, size=min(len(kept), 2048), replace=False))
+    idx = inp["topk_idx"].reshape(-1).cpu().numpy()[pairs]
+    g = _np(inp["g"].index_select(0, torch.as_tensor(pairs // k, device="cuda"))).astype(np.float64)
+    phi = _np(inp["phi"].reshape(T * k, I).index_select(0, torch.as_tensor(pairs, device="cuda")))
+    want = np.zeros(len(pairs))
+    for e in np.unique(idx):
+        sel = np.nonzero(idx == e)[0]
+        wd = _np(inp["w_down"][int(e)])[None]
+        # one pseudo-token per pair (k = 1), all retained, expert index 0 of the one-expert weights
+        want[sel] = oracle.router_grad(np.zeros(len(sel), np.int64), np.zeros((len(sel), 1), np.int64),
+                                       g[sel], phi[sel].astype(np.float64), wd)
+    assert rel_fro(dalpha[pairs], want) <= TOL[wl.dtype], (name, rel_fro(dalpha[pairs], want))

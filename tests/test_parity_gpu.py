@@ -94,6 +94,48 @@ def test_small_parity(wl):
         full_check(wl, inp, loads, q, pb)
 
 
+def check_router_grad(wl, inp, pb):
+    """dL/dalpha against the oracle on the GPU's own selection; dropped pairs exactly 0; row_dot of
+    row r equals alpha_u * dalpha_u of its pair."""
+    tol = TOL[wl.dtype]
+    cpu = {n: v.cpu() for n, v in inp.items()}
+    P = wl.P
+    rop = to_np(pb.row_of_pair)[:P]
+    want = oracle.router_grad(rop, to_np(cpu["topk_idx"]), to_np(cpu["g"]), to_np(cpu["phi"]),
+                              to_np(cpu["w_down"]))
+    got = to_np(pb.dalpha)[:P]
+    assert np.all(got[rop < 0] == 0)
+    kept = rop >= 0
+    if kept.any():
+        assert rel_fro(got[kept], want[kept]) <= tol, rel_fro(got[kept], want[kept])
+        alpha = to_np(cpu["alpha"]).reshape(-1)
+        rd = to_np(pb.row_dot)[rop[kept]]
+        assert rel_fro(rd, alpha[kept] * want[kept]) <= tol
+
+
+@pytest.mark.parametrize("wl", SMALL, ids=lambda w: w.name)
+def test_router_grad_parity(wl):
+    for flags in GEMM_MODES[wl.dtype]:
+        inp, loads, q, pb = run_cuda_path(wl, seed=2, flags=flags, router_grad=True)
+        assert int(pb.dev_status.item()) == 0
+        check_router_grad(wl, inp, pb)
+        # the other outputs are unchanged by the extra epilogue work
+        full_check(wl, inp, loads, q, pb)
+
+
+def test_router_grad_edges():
+    wl = W.small_workload("router_edges", 400, 256, 136, 8, 2)
+    for flags in GEMM_MODES["bf16"]:
+        # nothing kept: every dalpha is 0
+        inp, loads, q, pb = run_cuda_path(wl, flags=flags, quotas=np.zeros(8, np.int32), router_grad=True)
+        assert int(pb.dev_status.item()) == 0
+        assert torch.all(pb.dalpha == 0)
+        # everything kept: the unpruned router gradient
+        inp, loads, q, pb = run_cuda_path(wl, flags=flags, quotas=np.full(8, 10 ** 6, np.int32), router_grad=True)
+        assert int(pb.seg_offsets[-1]) == wl.P
+        check_router_grad(wl, inp, pb)
+
+
 def test_load_example():
     wl = W.WORKLOADS["load_example"]
     inp, loads, q, pb = run_cuda_path(wl, flags=SIMT)
