@@ -77,6 +77,50 @@ def plan_quotas(topk_idx, E, kind, num=0, den=1, cap=0, explicit=None):
 
 
 # ----------------------------------------------------------------------------------------
+# forward-side steps beside the path  ([EN] "Backward demand is not a constant": the controller
+# fixes each expert's quota from its routed demand before the expert forward, so the quota rule
+# can run where the routing is decided; [EN] "LRM: a decomposable contribution score": the score
+# needs only ||phi_u||^2 of the saved projection input, a number the forward can emit while it
+# forms phi)
+# ----------------------------------------------------------------------------------------
+def route(logits, k):
+    """Top-k routing of every token: the k largest logits in descending order (ties to the lower
+    expert id) and alpha = softmax over those k logits, in fp64.
+    Pinned: brute-force ranking on small integer logits full of ties; alpha sums to 1, follows the
+    logit order, and for k = 2 equals the logistic function of the logit gap."""
+    L = np.asarray(logits, dtype=np.float64)
+    T, E = L.shape
+    idx = np.zeros((T, k), dtype=np.int64)
+    alpha = np.zeros((T, k))
+    for t in range(T):
+        order = np.lexsort((np.arange(E), -L[t]))   # logit descending, then expert id ascending
+        idx[t] = order[:k]
+        chosen = L[t, idx[t]]
+        w = np.exp(chosen - chosen[0])
+        alpha[t] = w / w.sum()
+    return idx, alpha
+
+
+def swiglu_forward(h, I):
+    """Rows h = [gate ; up] (2I) -> phi = SiLU(gate) * up = gate * sigmoid(gate) * up (fp64) and
+    phi_sq = ||phi||_2^2 of every row.
+    Pinned: torch fp64 silu; the derivative of this phi is what swiglu_backward returns."""
+    H2 = np.asarray(h, dtype=np.float64)
+    gate, up = H2[..., :I], H2[..., I:]
+    phi = gate * sigmoid(gate) * up
+    return phi, np.sum(phi * phi, axis=-1)
+
+
+def lrm_scores_from_norms(alpha, g, phi_sq):
+    """R[t, j] = alpha[t,j]^2 * ||g_t||_2^2 * phi_sq[t,j]: the LRM score with ||phi_u||^2 handed in.
+    Pinned: equals lrm_scores when phi_sq = ||phi_u||^2."""
+    a = np.asarray(alpha, dtype=np.float64)
+    G = np.asarray(g, dtype=np.float64)
+    g2 = np.sum(G * G, axis=1)
+    return a * a * g2[:, None] * np.asarray(phi_sq, dtype=np.float64)
+
+
+# ----------------------------------------------------------------------------------------
 # LRM score  ([EN] "LRM: a decomposable contribution score": G_u = (alpha_u g_t) phi_u^T is
 # rank one, so ||G_u||_F^2 splits into routing strength alpha_u^2, backward signal
 # ||g_t||^2 and expert-state magnitude ||phi_u||^2; [PT] "Seleção pela métrica LRM")

@@ -259,6 +259,81 @@ def test_router_grad_pruned_equals_masked_route():
     assert err < 1e-12
 
 
+def route_pin_mismatches(route_fn, trials=200, seed=5):
+    """Brute-force ranking: expert e's rank is the number of experts with a larger logit or an
+    equal logit and a smaller id; the top-k are ranks 0..k-1 in rank order."""
+    rng = np.random.default_rng(seed)
+    bad = 0
+    for _ in range(trials):
+        T, E = int(rng.integers(1, 5)), int(rng.integers(1, 9))
+        k = int(rng.integers(1, E + 1))
+        L = rng.integers(-2, 3, (T, E)).astype(np.float64)   # small integers: ties everywhere
+        idx, alpha = route_fn(L, k)
+        for t in range(T):
+            rank = [sum(1 for f in range(E) if L[t, f] > L[t, e] or (L[t, f] == L[t, e] and f < e))
+                    for e in range(E)]
+            want = sorted(range(E), key=lambda e: rank[e])[:k]
+            if list(idx[t]) != want:
+                bad += 1
+    return bad
+
+
+def route_alpha_pin_error(route_fn, seed=6):
+    rng = np.random.default_rng(seed)
+    L = rng.normal(0, 2, (50, 6))
+    idx, alpha = route_fn(L, 2)
+    gap = np.take_along_axis(L, idx, 1)
+    logistic = 1.0 / (1.0 + np.exp(-(gap[:, 0] - gap[:, 1])))
+    err = np.max(np.abs(alpha[:, 0] - logistic))
+    idx4, alpha4 = route_fn(L, 4)
+    err = max(err, np.max(np.abs(alpha4.sum(1) - 1.0)))
+    assert np.all(np.diff(alpha4, axis=1) <= 0)
+    return err
+
+
+def test_route_ranks_by_brute_force():
+    assert route_pin_mismatches(O.route) == 0
+
+
+def test_route_alpha_closed_forms():
+    assert route_alpha_pin_error(O.route) < 1e-14
+
+
+def swiglu_forward_pin_error(seed=7):
+    rng = np.random.default_rng(seed)
+    I = 9
+    h = rng.normal(0, 3, (20, 2 * I))
+    phi, phi_sq = O.swiglu_forward(h, I)
+    ht = torch.tensor(h, dtype=torch.float64)
+    want = torch.nn.functional.silu(ht[:, :I]) * ht[:, I:]
+    err = np.max(np.abs(phi - want.numpy()))
+    err = max(err, np.max(np.abs(phi_sq - (want * want).sum(1).numpy()) / (want * want).sum(1).numpy()))
+    # the derivative of this phi is the backward closed form (central differences)
+    eps = 1e-6
+    dphi = rng.normal(0, 1, (20, I))
+    hp, hm = h.copy(), h.copy()
+    hp[:, :I] += eps
+    hm[:, :I] -= eps
+    fd_gate = dphi * (O.swiglu_forward(hp, I)[0] - O.swiglu_forward(hm, I)[0]) / (2 * eps)
+    dgate, _ = O.swiglu_backward(dphi, h[:, :I], h[:, I:])
+    return err, np.max(np.abs(fd_gate - dgate))
+
+
+def test_swiglu_forward_matches_torch_and_backward():
+    err, fd = swiglu_forward_pin_error()
+    assert err < 1e-12 and fd < 1e-5
+
+
+def test_scores_from_norms_equal_lrm_scores():
+    rng = np.random.default_rng(8)
+    alpha = rng.uniform(0.05, 1.0, (6, 3))
+    g = rng.normal(0, 1, (6, 11))
+    phi = rng.normal(0, 1, (6, 3, 5))
+    want = O.lrm_scores(alpha, g, phi)
+    got = O.lrm_scores_from_norms(alpha, g, np.sum(phi * phi, axis=2))
+    assert np.max(np.abs(got - want) / want) < 1e-14
+
+
 def test_compacted_equals_zero_masked_full_shape():
     assert masking_pin_error() < 1e-12
 
@@ -359,6 +434,23 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     with monkeypatch.context() as m:
         m.setattr(O, "scatter_dx", _planted_scatter_drops_last_choice)
         assert autograd_pin_error() > 1e-3
+    # forward-side steps
+    def route_ties_to_higher_id(L, k):
+        idx, alpha = O.route(np.asarray(L)[:, ::-1], k)
+        return np.asarray(L).shape[1] - 1 - idx, alpha
+
+    def route_softmax_over_all(L, k):
+        idx, _ = O.route(L, k)
+        L = np.asarray(L, np.float64)
+        w = np.exp(L - L.max(1, keepdims=True))
+        return idx, np.take_along_axis(w / w.sum(1, keepdims=True), idx, 1)
+
+    assert route_pin_mismatches(route_ties_to_higher_id) > 0
+    assert route_alpha_pin_error(route_softmax_over_all) > 1e-3
+    real_sigmoid = O.sigmoid
+    with monkeypatch.context() as m:
+        m.setattr(O, "sigmoid", lambda z: real_sigmoid(2 * z))
+        assert swiglu_forward_pin_error()[0] > 1e-3
     real_router = O.router_grad
 
     def router_scaled_by_alpha(rop, idx, g, phi, w_down, pairs=None):

@@ -88,7 +88,8 @@ def generate(wl: Workload, device="cpu", seed: int = 0) -> dict:
     Draw order: router noise [T,E], x [T,H], g [T,H], W_gate_up [E,2I,H], W_down [E,H,I].
     Returns a dict of tensors on `device`:
       topk_idx int32 [T,k], alpha fp32 [T,k], x [T,H], g [T,H], h [T,k,2I] (gate first),
-      phi [T,k,I], w_gate_up [E,2I,H], w_down [E,H,I]; the last six in wl.dtype.
+      phi [T,k,I], w_gate_up [E,2I,H], w_down [E,H,I] (the last six in wl.dtype), and the fp32
+      router logits [T,E] the top-k was taken from (noise + bias; plain noise for an explicit routing).
     """
     dev = torch.device(device)
     gen = torch.Generator(device=dev)
@@ -99,6 +100,7 @@ def generate(wl: Workload, device="cpu", seed: int = 0) -> dict:
     # Router: logits N(0,1) plus log of Zipf(s) popularity (expert 0 hottest); the
     # top-k biased logits choose the experts and their softmax gives alpha.
     noise = _randn(gen, (T, E), dev)
+    logits = noise
     if wl.topk_idx is not None:
         topk_idx = torch.tensor(wl.topk_idx, dtype=torch.int64, device=dev).view(T, k)
         chosen = torch.gather(noise, 1, topk_idx)
@@ -142,6 +144,7 @@ def generate(wl: Workload, device="cpu", seed: int = 0) -> dict:
         "phi": phi.view(T, k, I).contiguous(),
         "w_gate_up": w_gate_up.contiguous(),
         "w_down": w_down.contiguous(),
+        "logits": logits.contiguous(),
     }
 
 
