@@ -342,6 +342,7 @@ def main():
     if tr:
         roof["traffic_workload"] = tr["workload"]
 
+    nxt = next_rows(args, wl, inp, quotas, flags, dev, stream, ms_per_step, pk)
     launches = pb_launches(wl, flags)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -357,6 +358,7 @@ def main():
         "e2e": e2e,
         "gpu_launches": launches * args.steps,
         "clocks": clk,
+        "next_rows": nxt,
     }
     if not args.no_cpu_baseline and world == 1:
         cpu_inp = {n: v.cpu() for n, v in inp.items()}
@@ -368,6 +370,95 @@ def main():
     print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
+
+
+def _event_ms(fn, n, stream):
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(n):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / n
+
+
+def _graph_ms(fn, n, stream, reps=20):
+    """Per-call device time of a short launch sequence: `reps` calls captured in one CUDA graph,
+    replayed n times (host launch overhead would otherwise dominate microsecond kernels)."""
+    for _ in range(3):
+        fn()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            fn()
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(n):
+        g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / (n * reps)
+
+
+def next_rows(args, wl, inp, quotas, flags, dev, stream, ms_step, pk):
+    """Widened rows, timed apart from the headline step (same inputs, same stream): the step with
+    the routing-weight gradient added (fused dphi . phi parts, their ordered sum, and the division /
+    return to pair order), the forward-side steps (router with quotas, SwiGLU with row norms, score
+    from norms) and the gradient-only ablation scores."""
+    import pruned_expert_backward_gb300 as lrm
+    n = max(10, min(args.steps, 50))
+    pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, device=dev, flags=flags,
+                            router_grad=True)
+    ms_rg = _event_ms(lambda: pb.run(inp, quotas), n, stream)
+    ms_rk = _graph_ms(lambda: lrm.lrm_router_grad(pb.row_of_pair, inp["alpha"], pb.row_dot, wl.T, wl.k, pb.cap,
+                                                  dalpha=pb.dalpha), n, stream)
+    st = int(pb.dev_status.item())
+    del pb
+    b = 2 if wl.dtype == "bf16" else 4
+    out = {"router_grad": {"ms_per_step": round(ms_rg, 4), "added_ms": round(ms_rg - ms_step, 4),
+                           "router_grad_kernel_ms": round(ms_rk, 4), "steps": n, "dev_status": st}}
+    scores = torch.empty(wl.P, dtype=torch.float32, device=dev)
+
+    def hbm(ms, by):
+        gbs = by / (ms / 1e3) / 1e9
+        return {"ms": round(ms, 4), "alg_bytes": by, "GB/s": round(gbs, 1), "frac_hbm": round(gbs / pk["hbm_gbs"], 4)}
+
+    # forward-side steps: router top-k with loads and quotas in one launch, SwiGLU activation that
+    # also emits ||phi||^2, and the score from those norms (phi not re-read)
+    kind, num, den, cap, expl = W.quota_policy(wl)
+    ex = None if expl is None else torch.tensor(expl, dtype=torch.int32, device=dev)
+    ws = torch.empty(64, dtype=torch.uint8, device=dev)
+    r_out = [torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev),
+             torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev),
+             torch.empty(wl.E, dtype=torch.int32, device=dev), torch.empty(wl.E, dtype=torch.int32, device=dev)]
+    ms = _graph_ms(lambda: lrm.lrm_route(inp["logits"], wl.k, kind, num, den, cap, explicit=ex, topk_idx=r_out[0],
+                                         alpha=r_out[1], loads=r_out[2], quotas=r_out[3], ws=ws), n, stream)
+    out["route_with_quotas"] = hbm(ms, 4 * wl.T * wl.E + 8 * wl.P + 8 * wl.E)
+    out["route_with_quotas"]["matches_generator_routing"] = bool(torch.equal(r_out[0], inp["topk_idx"]))
+    phi = torch.empty_like(inp["phi"])
+    phi_sq = torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev)
+    ms = _graph_ms(lambda: lrm.lrm_swiglu_forward(inp["h"], phi=phi, phi_sq=phi_sq), n, stream)
+    out["swiglu_forward_with_norms"] = hbm(ms, wl.P * 3 * wl.I * b + 4 * wl.P)
+    ms = _graph_ms(lambda: lrm.lrm_swiglu_forward(inp["h"], phi=phi, norms=False), n, stream)
+    out["swiglu_forward_without_norms"] = hbm(ms, wl.P * 3 * wl.I * b)
+    ms = _graph_ms(lambda: lrm.lrm_score_norms(inp["alpha"], inp["g"], phi_sq, scores=scores), n, stream)
+    out["score_from_norms"] = hbm(ms, wl.T * wl.H * b + 12 * wl.P)
+    for name in ("grad_sq", "grad_abs"):
+        ms = _graph_ms(lambda: lrm.lrm_score_mode(inp["alpha"], inp["g"], inp["phi"], name, scores=scores), n,
+                       stream)
+        by = wl.T * wl.H * b + 4 * wl.P
+        out[f"score_{name}"] = {"ms": round(ms, 4), "alg_bytes": by,
+                                "GB/s": round(by / (ms / 1e3) / 1e9, 1),
+                                "frac_hbm": round(by / (ms / 1e3) / 1e9 / pk["hbm_gbs"], 4)}
+    return out
 
 
 def pb_launches(wl, flags):

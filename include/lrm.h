@@ -220,6 +220,47 @@ lrm_status lrm_router_grad(const int32_t* row_of_pair, const float* alpha, const
 lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,
                           lrm_dtype dt, void* dx, cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------------
+ * Forward-side steps beside the path, each fused with the work next to it.
+ * ------------------------------------------------------------------------------------------- */
+
+/*
+ * Router top-k with the loads and quotas in the same launch ("Backward demand is not a constant":
+ * each expert's quota is fixed from its routed demand before the expert forward; here it is
+ * computed where the routing is decided, replacing a separate lrm_plan_quotas pass).
+ *   logits [T,E] fp32 (row-major)  ->  topk_idx [T*k] int32: the k largest logits of each token in
+ *   descending order, ties to the lower expert id; alpha [T*k] fp32: softmax over those k logits;
+ *   loads [E], quotas [E] int32 exactly as lrm_plan_quotas writes them for this routing.
+ *   kind/num/den/cap/explicit_quotas as in lrm_plan_quotas.
+ *   ws: any 4-byte-aligned device scratch of >= 4 bytes (a buffer of lrm_workspace_size bytes does).
+ * A non-finite logit is never chosen ahead of a finite one and sets LRM_ERR_NONFINITE in
+ * dev_status.  Integer results are deterministic.  Errors: LRM_ERR_INVALID_ARG, LRM_ERR_SHAPE
+ * (also k > E), LRM_ERR_WORKSPACE, LRM_ERR_CUDA.
+ */
+lrm_status lrm_route(const float* logits, int64_t T, int32_t E, int32_t k, lrm_quota_kind kind, int32_t num,
+                     int32_t den, int32_t cap, const int32_t* explicit_quotas, int32_t* topk_idx, float* alpha,
+                     int32_t* loads, int32_t* quotas, void* ws, size_t ws_bytes, int32_t* dev_status,
+                     cudaStream_t stream);
+
+/*
+ * SwiGLU activation of the expert forward, also emitting the row norms the LRM score needs
+ * ("LRM: a decomposable contribution score": only ||phi_u||^2 of the saved projection input
+ * enters the score, so the forward can hand it over and the backward need not re-read phi).
+ *   h [P, 2I] dt (gate first)  ->  phi [P, I] dt = round_dt(SiLU(gate) * up) (fp32 arithmetic),
+ *   phi_sq [P] fp32 = ||phi_u||^2 of the stored (rounded) row, or NULL to skip it.
+ * Errors: LRM_ERR_INVALID_ARG (NULL or misaligned h/phi), LRM_ERR_SHAPE, LRM_ERR_DTYPE, LRM_ERR_CUDA.
+ */
+lrm_status lrm_swiglu_forward(const void* h, int64_t P, int32_t I, lrm_dtype dt, void* phi, float* phi_sq,
+                              cudaStream_t stream);
+
+/*
+ * LRM score from the forward's row norms: scores[u] = alpha_u^2 * ||g_t||^2 * phi_sq[u], the value
+ * lrm_score computes, with phi_sq [T*k] fp32 in place of phi.  Reads g once per token and never
+ * reads phi.  Same errors and non-finite flag as lrm_score.
+ */
+lrm_status lrm_score_norms(const float* alpha, const void* g, const float* phi_sq, int64_t T, int32_t k,
+                           int32_t H, lrm_dtype dt, float* scores, int32_t* dev_status, cudaStream_t stream);
+
 /*
  * Self-test of failure detection (no counterpart in the pages; part of this library's fault
  * handling).  The tensor-core kernels bound every wait on an mbarrier (about one second of

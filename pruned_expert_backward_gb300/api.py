@@ -86,6 +86,54 @@ def lrm_score(alpha, g, phi, scores=None, dev_status=None):
     return scores
 
 
+def lrm_score_norms(alpha, g, phi_sq, scores=None, dev_status=None):
+    """LRM score from the forward's ||phi_u||^2 (phi_sq fp32 [T,k] or [T*k]); phi is not read."""
+    T, H = g.shape
+    k = alpha.numel() // max(T, 1) if T > 0 else alpha.shape[-1]
+    if phi_sq.numel() != alpha.numel():
+        raise ValueError("alpha and phi_sq must both hold T*k values")
+    scores = torch.empty(T * k, dtype=torch.float32, device=g.device) if scores is None else scores
+    _ok(L.load().lrm_score_norms(_cuda(alpha, "alpha", torch.float32), _cuda(g, "g"),
+                                 _cuda(phi_sq, "phi_sq", torch.float32), T, k, H, _dt(g),
+                                 _cuda(scores, "scores", torch.float32), _opt(dev_status, "dev_status", torch.int32),
+                                 _stream()), "lrm_score_norms")
+    return scores
+
+
+def lrm_route(logits, k, kind, num=0, den=1, cap=0, explicit=None, topk_idx=None, alpha=None, loads=None,
+              quotas=None, ws=None, dev_status=None):
+    """Router top-k + softmax weights + loads + quotas in one launch.  logits fp32 [T,E].
+    Returns topk_idx int32 [T,k], alpha fp32 [T,k], loads int32 [E], quotas int32 [E]."""
+    T, E = logits.shape
+    dev = logits.device
+    i32 = dict(dtype=torch.int32, device=dev)
+    topk_idx = torch.empty(T, k, **i32) if topk_idx is None else topk_idx
+    alpha = torch.empty(T, k, dtype=torch.float32, device=dev) if alpha is None else alpha
+    loads = torch.empty(E, **i32) if loads is None else loads
+    quotas = torch.empty(E, **i32) if quotas is None else quotas
+    ws = torch.empty(64, dtype=torch.uint8, device=dev) if ws is None else ws
+    kinds = {"ratio": L.LRM_QUOTA_RATIO, "cap": L.LRM_QUOTA_CAP, "explicit": L.LRM_QUOTA_EXPLICIT}
+    _ok(L.load().lrm_route(_cuda(logits, "logits", torch.float32), T, E, k, kinds[kind], num, den, cap,
+                           _opt(explicit, "explicit", torch.int32), _cuda(topk_idx, "topk_idx", torch.int32),
+                           _cuda(alpha, "alpha", torch.float32), _cuda(loads, "loads", torch.int32),
+                           _cuda(quotas, "quotas", torch.int32), _cuda(ws, "ws"), ws.numel(),
+                           _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_route")
+    return topk_idx, alpha, loads, quotas
+
+
+def lrm_swiglu_forward(h, phi=None, phi_sq=None, norms=True):
+    """phi = SiLU(gate) * up of rows h [..., 2I] (gate first), plus ||phi||^2 per row when norms."""
+    I = h.shape[-1] // 2
+    P = h.numel() // (2 * I)
+    phi = torch.empty(*h.shape[:-1], I, dtype=h.dtype, device=h.device) if phi is None else phi
+    if norms and phi_sq is None:
+        phi_sq = torch.empty(h.shape[:-1], dtype=torch.float32, device=h.device)
+    _ok(L.load().lrm_swiglu_forward(_cuda(h, "h"), P, I, _dt(h), _cuda(phi, "phi", h.dtype),
+                                    _opt(phi_sq if norms else None, "phi_sq", torch.float32), _stream()),
+        "lrm_swiglu_forward")
+    return phi, (phi_sq if norms else None)
+
+
 def lrm_score_mode(alpha, g, phi, mode, scores=None, dev_status=None):
     """mode: "lrm", "grad_sq" (||g_t||^2) or "grad_abs" (||g_t||_1); phi gives k and I."""
     T, H = g.shape
@@ -212,8 +260,12 @@ class PrunedBackward:
 
     def run(self, inp, quotas):
         """inp: dict with topk_idx [T,k] int32, alpha [T,k] fp32, x, g [T,H], h [T,k,2I], phi [T,k,I],
-        w_gate_up [E,2I,H], w_down [E,H,I] (CUDA).  quotas: int32 [E] (CUDA)."""
-        lrm_score(inp["alpha"], inp["g"], inp["phi"], scores=self.scores, dev_status=self.dev_status)
+        w_gate_up [E,2I,H], w_down [E,H,I] (CUDA), and optionally phi_sq fp32 [T,k] (||phi_u||^2 from
+        lrm_swiglu_forward; the score then reads it instead of phi).  quotas: int32 [E] (CUDA)."""
+        if inp.get("phi_sq") is not None:  # the forward handed over ||phi_u||^2
+            lrm_score_norms(inp["alpha"], inp["g"], inp["phi_sq"], scores=self.scores, dev_status=self.dev_status)
+        else:
+            lrm_score(inp["alpha"], inp["g"], inp["phi"], scores=self.scores, dev_status=self.dev_status)
         lrm_select(inp["topk_idx"], self.scores, quotas, self.E, cap=self.cap, seg_offsets=self.seg_offsets,
                    kept_pair=self.kept_pair, row_of_pair=self.row_of_pair, ws=self.ws, dev_status=self.dev_status)
         lrm_compact(self.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], self.cap,

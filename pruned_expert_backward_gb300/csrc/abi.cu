@@ -119,6 +119,51 @@ lrm_status lrm_score(const float* alpha, const void* g, const void* phi, int64_t
   return after_launch();
 }
 
+lrm_status lrm_score_norms(const float* alpha, const void* g, const float* phi_sq, int64_t T, int32_t k, int32_t H,
+                           lrm_dtype dt, float* scores, int32_t* dev_status, cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, 1, H, 8);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (T > 0 && (!alpha || !g || !phi_sq || !scores)) return LRM_ERR_INVALID_ARG;
+  if (!al16(g)) return LRM_ERR_INVALID_ARG;
+  launch_score_norms(alpha, g, phi_sq, T, k, H, dt, scores, dev_status, stream);
+  return after_launch();
+}
+
+lrm_status lrm_route(const float* logits, int64_t T, int32_t E, int32_t k, lrm_quota_kind kind, int32_t num,
+                     int32_t den, int32_t cap, const int32_t* explicit_quotas, int32_t* topk_idx, float* alpha,
+                     int32_t* loads, int32_t* quotas, void* ws, size_t ws_bytes, int32_t* dev_status,
+                     cudaStream_t stream) {
+  lrm_status st = check_dims(T, k, E, 8, 8);
+  if (st) return st;
+  if (k > E) return LRM_ERR_SHAPE;
+  if (!loads || !quotas) return LRM_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_idx || !alpha)) return LRM_ERR_INVALID_ARG;
+  if (kind == LRM_QUOTA_RATIO) {
+    if (num <= 0 || den <= 0) return LRM_ERR_INVALID_ARG;
+  } else if (kind == LRM_QUOTA_CAP) {
+    if (cap < 0) return LRM_ERR_INVALID_ARG;
+  } else if (kind == LRM_QUOTA_EXPLICIT) {
+    if (!explicit_quotas) return LRM_ERR_INVALID_ARG;
+  } else {
+    return LRM_ERR_INVALID_ARG;
+  }
+  if (!ws || ws_bytes < sizeof(uint32_t) || (reinterpret_cast<uintptr_t>(ws) & 3u)) return LRM_ERR_WORKSPACE;
+  return launch_route(logits, T, E, k, (int)kind, num, den, cap, explicit_quotas, topk_idx, alpha, loads, quotas,
+                      static_cast<uint32_t*>(ws), dev_status, stream);
+}
+
+lrm_status lrm_swiglu_forward(const void* h, int64_t P, int32_t I, lrm_dtype dt, void* phi, float* phi_sq,
+                              cudaStream_t stream) {
+  lrm_status st = check_dims(P, 1, 1, 8, I);
+  if (st) return st;
+  if ((st = check_dt(dt))) return st;
+  if (P > 0 && (!h || !phi)) return LRM_ERR_INVALID_ARG;
+  if (!al16(h) || !al16(phi)) return LRM_ERR_INVALID_ARG;
+  launch_swiglu_forward(h, P, I, dt, phi, phi_sq, stream);
+  return after_launch();
+}
+
 lrm_status lrm_score_mode(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H,
                           int32_t I, lrm_dtype dt, lrm_score_kind mode, float* scores, int32_t* dev_status,
                           cudaStream_t stream) {

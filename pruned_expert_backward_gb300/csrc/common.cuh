@@ -63,6 +63,19 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// The fixed quota rules of lrm_quota_kind for one expert with load l (exact integer arithmetic).
+__device__ __forceinline__ int32_t quota_rule(int64_t l, int kind, int32_t num, int32_t den, int32_t cap,
+                                              const int32_t* explicit_q, int e) {
+  int64_t q;
+  if (kind == LRM_QUOTA_RATIO)
+    q = ((int64_t)num * l + den - 1) / den;  // ceil(num/den * load)
+  else if (kind == LRM_QUOTA_CAP)
+    q = l < cap ? l : cap;
+  else
+    q = explicit_q[e];
+  return (int32_t)(q > INT32_MAX ? INT32_MAX : q);
+}
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 template <typename T> __device__ __forceinline__ T from_f(float v);

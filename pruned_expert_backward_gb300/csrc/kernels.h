@@ -43,6 +43,16 @@ void launch_plan_quotas(const int32_t* topk_idx, int64_t P, int32_t E, int kind,
 void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
                   lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s);
 
+void launch_score_norms(const float* alpha, const void* g, const float* phi_sq, int64_t T, int32_t k, int32_t H,
+                        lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s);
+
+lrm_status launch_route(const float* logits, int64_t T, int32_t E, int32_t k, int kind, int32_t num, int32_t den,
+                        int32_t cap, const int32_t* explicit_q, int32_t* topk_idx, float* alpha, int32_t* loads,
+                        int32_t* quotas, uint32_t* done, int32_t* status, cudaStream_t s);
+
+void launch_swiglu_forward(const void* h, int64_t P, int32_t I, lrm_dtype dt, void* phi, float* phi_sq,
+                           cudaStream_t s);
+
 void launch_grad_score(const void* g, int64_t T, int32_t k, int32_t H, lrm_dtype dt, bool abs_mode, float* scores,
                        int32_t* status, cudaStream_t s);
 

@@ -30,17 +30,7 @@ __global__ void __launch_bounds__(256) load_hist_kernel(const int32_t* __restric
 
 __global__ void quota_rule_kernel(const int32_t* __restrict__ loads, int E, int kind, int32_t num, int32_t den,
                                   int32_t cap, const int32_t* __restrict__ explicit_q, int32_t* __restrict__ quotas) {
-  for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int64_t l = loads[e];
-    int64_t q;
-    if (kind == LRM_QUOTA_RATIO)
-      q = ((int64_t)num * l + den - 1) / den;  // ceil(num/den * load), exact
-    else if (kind == LRM_QUOTA_CAP)
-      q = l < cap ? l : cap;
-    else
-      q = explicit_q[e];
-    quotas[e] = (int32_t)(q > INT32_MAX ? INT32_MAX : q);
-  }
+  for (int e = threadIdx.x; e < E; e += blockDim.x) quotas[e] = quota_rule(loads[e], kind, num, den, cap, explicit_q, e);
 }
 
 }  // namespace

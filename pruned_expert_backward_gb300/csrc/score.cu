@@ -13,9 +13,9 @@
 
 namespace lrm {
 
-// Per-lane partial sum of squares of one row of nv 16-byte vectors (v = lane, lane+32, ...):
-// all of the lane's loads are issued before any is used (at most MAXV per lane).
-template <typename T, int MAXV>
+// Per-lane partial sum of squares (ABS: of magnitudes) of one row of nv 16-byte vectors
+// (v = lane, lane+32, ...): all of the lane's loads are issued before any is used (at most MAXV).
+template <typename T, int MAXV, bool ABS = false>
 __device__ __forceinline__ float lane_sumsq(const T* row, int nv, int lane) {
   constexpr int VN = VecTraits<T>::N;
   uint4 buf[MAXV];
@@ -30,12 +30,12 @@ __device__ __forceinline__ float lane_sumsq(const T* row, int nv, int lane) {
     float f[VN];
     unpack(buf[m], f);
 #pragma unroll
-    for (int q = 0; q < VN; ++q) acc = fmaf(f[q], f[q], acc);
+    for (int q = 0; q < VN; ++q) acc = ABS ? acc + fabsf(f[q]) : fmaf(f[q], f[q], acc);
   }
   return acc;
 }
 // Same, for rows of any length (a loop; used when a row exceeds MAXV vectors per lane).
-template <typename T>
+template <typename T, bool ABS = false>
 __device__ __forceinline__ float lane_sumsq_any(const T* row, int nv, int lane) {
   constexpr int VN = VecTraits<T>::N;
   float acc = 0.f;
@@ -43,7 +43,7 @@ __device__ __forceinline__ float lane_sumsq_any(const T* row, int nv, int lane) 
     float f[VN];
     unpack(ld_stream16(row + (int64_t)v * VN), f);
 #pragma unroll
-    for (int q = 0; q < VN; ++q) acc = fmaf(f[q], f[q], acc);
+    for (int q = 0; q < VN; ++q) acc = ABS ? acc + fabsf(f[q]) : fmaf(f[q], f[q], acc);
   }
   return acc;
 }
@@ -91,11 +91,52 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ al
   }
 }
 
+// The same score with ||phi_u||^2 handed in (from a forward that emits it, see forward.cu): one
+// warp per token reads g_t once and writes its k scores; phi itself is not read.
+template <typename T, int GV>
+__global__ void __launch_bounds__(256) score_norms_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
+                                                         const float* __restrict__ phi_sq, int64_t n_tok, int k,
+                                                         int H, float* __restrict__ scores, int32_t* status) {
+  constexpr int VN = VecTraits<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= n_tok) return;
+  float a = 0.f, p = 0.f;
+  if (lane < k) {  // issued before the g loads complete
+    a = alpha[t * k + lane];
+    p = phi_sq[t * k + lane];
+  }
+  float gs = GV ? lane_sumsq<T, (GV ? GV : 1)>(g + t * H, H / VN, lane) : lane_sumsq_any<T>(g + t * H, H / VN, lane);
+  gs = warp_sum(gs);
+  if (lane < k) {
+    const float sc = (a * a) * gs * p;
+    scores[t * k + lane] = sc;
+    if (!isfinite(sc)) set_status(status, LRM_ERR_NONFINITE);
+  }
+}
+
+void launch_score_norms(const float* alpha, const void* g, const float* phi_sq, int64_t T, int32_t k, int32_t H,
+                        lrm_dtype dt, float* scores, int32_t* status, cudaStream_t s) {
+  if (T == 0) return;
+  const unsigned blocks = (unsigned)((T + 7) / 8);
+  const int gv = (H / (dt == LRM_BF16 ? 8 : 4) + 31) / 32;
+  using B = __nv_bfloat16;
+  if (dt == LRM_BF16) {
+    if (gv <= 16) score_norms_kernel<B, 16><<<blocks, 256, 0, s>>>(alpha, (const B*)g, phi_sq, T, k, H, scores, status);
+    else score_norms_kernel<B, 0><<<blocks, 256, 0, s>>>(alpha, (const B*)g, phi_sq, T, k, H, scores, status);
+  } else {
+    if (gv <= 16)
+      score_norms_kernel<float, 16><<<blocks, 256, 0, s>>>(alpha, (const float*)g, phi_sq, T, k, H, scores, status);
+    else
+      score_norms_kernel<float, 0><<<blocks, 256, 0, s>>>(alpha, (const float*)g, phi_sq, T, k, H, scores, status);
+  }
+}
+
 // Gradient-only ablation scores ("LRMoE: Trimming Backward Work in Memory-Bound MoE Training",
 // section "What the measurements show": squared gradient norm and absolute gradient magnitude):
 // one warp per token computes ||g_t||_2^2 (ABS = false) or ||g_t||_1 (ABS = true) and writes it
 // to the token's k pairs.
-template <typename T, bool ABS>
+template <typename T, bool ABS, int GV>
 __global__ void __launch_bounds__(256) grad_score_kernel(const T* __restrict__ g, int64_t n_tok, int k, int H,
                                                          float* __restrict__ scores, int32_t* status) {
   constexpr int VN = VecTraits<T>::N;
@@ -103,14 +144,7 @@ __global__ void __launch_bounds__(256) grad_score_kernel(const T* __restrict__ g
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   if (t >= n_tok) return;
   const T* gt = g + t * H;
-  float acc = 0.f;
-#pragma unroll 8
-  for (int v = lane; v < H / VN; v += 32) {
-    float f[VN];
-    unpack(ld_stream16(gt + (int64_t)v * VN), f);
-#pragma unroll
-    for (int q = 0; q < VN; ++q) acc = ABS ? acc + fabsf(f[q]) : fmaf(f[q], f[q], acc);
-  }
+  float acc = GV ? lane_sumsq<T, (GV ? GV : 1), ABS>(gt, H / VN, lane) : lane_sumsq_any<T, ABS>(gt, H / VN, lane);
   acc = warp_sum(acc);
   if (lane < k) scores[t * k + lane] = acc;
   if (lane == 0 && !isfinite(acc)) set_status(status, LRM_ERR_NONFINITE);
@@ -120,15 +154,20 @@ void launch_grad_score(const void* g, int64_t T, int32_t k, int32_t H, lrm_dtype
                        int32_t* status, cudaStream_t s) {
   if (T == 0) return;
   const unsigned blocks = (unsigned)((T + 7) / 8);
+  const int gv = (H / (dt == LRM_BF16 ? 8 : 4) + 31) / 32;  // vectors per lane of a g row
   using B = __nv_bfloat16;
-  if (dt == LRM_BF16 && abs_mode)
-    grad_score_kernel<B, true><<<blocks, 256, 0, s>>>((const B*)g, T, k, H, scores, status);
-  else if (dt == LRM_BF16)
-    grad_score_kernel<B, false><<<blocks, 256, 0, s>>>((const B*)g, T, k, H, scores, status);
-  else if (abs_mode)
-    grad_score_kernel<float, true><<<blocks, 256, 0, s>>>((const float*)g, T, k, H, scores, status);
-  else
-    grad_score_kernel<float, false><<<blocks, 256, 0, s>>>((const float*)g, T, k, H, scores, status);
+#define LRM_GRAD_LAUNCH(TYPE, ABS)                                                                      \
+  do {                                                                                                  \
+    if (gv <= 16)                                                                                       \
+      grad_score_kernel<TYPE, ABS, 16><<<blocks, 256, 0, s>>>((const TYPE*)g, T, k, H, scores, status); \
+    else                                                                                                \
+      grad_score_kernel<TYPE, ABS, 0><<<blocks, 256, 0, s>>>((const TYPE*)g, T, k, H, scores, status);  \
+  } while (0)
+  if (dt == LRM_BF16 && abs_mode) LRM_GRAD_LAUNCH(B, true);
+  else if (dt == LRM_BF16) LRM_GRAD_LAUNCH(B, false);
+  else if (abs_mode) LRM_GRAD_LAUNCH(float, true);
+  else LRM_GRAD_LAUNCH(float, false);
+#undef LRM_GRAD_LAUNCH
 }
 
 void launch_score(const float* alpha, const void* g, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,

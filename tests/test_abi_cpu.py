@@ -58,6 +58,17 @@ def test_workspace_size_and_host_validation():
     assert lib.lrm_workspace_size(0, 1, 4, 64, 32, 0, C.byref(small)) == 0
     assert lib.lrm_grouped_backward(fake, fake, fake, fake, fake, fake, fake, 4, 64, 32, 0, 1 << 20, fake, fake,
                                     fake, fake, fake, fake, small.value, 0, None, None) == 4
+    # forward-side entry points
+    assert lib.lrm_route(None, 16, 8, 2, 0, 8, 10, 0, None, fake, fake, fake, fake, fake, 64, None, None) == 1
+    assert lib.lrm_route(fake, 16, 8, 9, 0, 8, 10, 0, None, fake, fake, fake, fake, fake, 64, None, None) == 2
+    assert lib.lrm_route(fake, 16, 8, 2, 0, 0, 10, 0, None, fake, fake, fake, fake, fake, 64, None, None) == 1
+    assert lib.lrm_route(fake, 16, 8, 2, 2, 0, 1, 0, None, fake, fake, fake, fake, fake, 64, None, None) == 1
+    assert lib.lrm_route(fake, 16, 8, 2, 0, 8, 10, 0, None, fake, fake, fake, fake, None, 0, None, None) == 4
+    assert lib.lrm_swiglu_forward(None, 16, 32, 0, fake, None, None) == 1
+    assert lib.lrm_swiglu_forward(fake, 16, 30, 0, fake, None, None) == 2   # I not a multiple of 8
+    assert lib.lrm_swiglu_forward(C.c_void_p(0x1001), 16, 32, 0, fake, None, None) == 1
+    assert lib.lrm_score_norms(fake, fake, None, 16, 2, 64, 0, fake, None, None) == 1
+    assert lib.lrm_score_norms(fake, fake, fake, 16, 2, 64, 5, fake, None, None) == 3
     # router gradient: null pointers, negative cap
     assert lib.lrm_router_grad(None, fake, fake, 16, 2, 32, fake, None) == 1
     assert lib.lrm_router_grad(fake, fake, None, 16, 2, 32, fake, None) == 1
