@@ -421,10 +421,19 @@ def next_rows(args, wl, inp, quotas, flags, dev, stream, ms_step, pk):
     ms_rk = _graph_ms(lambda: lrm.lrm_router_grad(pb.row_of_pair, inp["alpha"], pb.row_dot, wl.T, wl.k, pb.cap,
                                                   dalpha=pb.dalpha), n, stream)
     st = int(pb.dev_status.item())
+    R = int(pb.seg_offsets[-1].item())
     del pb
     b = 2 if wl.dtype == "bf16" else 4
     out = {"router_grad": {"ms_per_step": round(ms_rg, 4), "added_ms": round(ms_rg - ms_step, 4),
                            "router_grad_kernel_ms": round(ms_rk, 4), "steps": n, "dev_status": st}}
+    # compaction-free variant: only dy_c is compacted; x / h / phi rows are gathered by index
+    pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, device=dev, flags=flags,
+                            compaction="gather")
+    ms_g = _event_ms(lambda: pb.run(inp, quotas), n, stream)
+    out["compaction_free"] = {"ms_per_step": round(ms_g, 4), "value": round(R / (ms_g / 1e3), 1), "unit": UNIT,
+                              "vs_materialised": round(ms_step / ms_g, 4), "steps": n,
+                              "dev_status": int(pb.dev_status.item())}
+    del pb
     scores = torch.empty(wl.P, dtype=torch.float32, device=dev)
 
     def hbm(ms, by):

@@ -158,7 +158,9 @@ lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_
  *   row_of_pair [T*k] int32 (from lrm_select), alpha [T*k] fp32, g [T,H], x [T,H],
  *   h [T*k, 2I], phi [T*k, I]  ->  dy_c [cap,H], x_c [cap,H], h_c [cap,2I], phi_c [cap,I] (dt).
  * Rows are visited token by token, so g_t and x_t are read once per token.  Rows >= cap are
- * skipped.
+ * skipped.  With x_c, h_c and phi_c all NULL only dy_c is written (x, h, phi may then be NULL):
+ * the compaction-free variant, whose grouped backward reads those rows in place
+ * (lrm_grouped_backward_gather).
  */
 lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x,
                        const void* h, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
@@ -193,6 +195,24 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
                                 int32_t H, int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up,
                                 float* dw_down, void* dh_c, void* dx_c, float* row_dot, void* ws,
                                 size_t ws_bytes, int32_t flags, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Compaction-free variant of lrm_grouped_backward (measured against the materialised compaction
+ * the pages insist on, "The part that is easy to get wrong"): the same products and outputs,
+ * with only dy_c compacted.  The rows of x, h and phi are read where they are, through the
+ * compacted-row -> pair map kept_pair from lrm_select: row r stands for pair u = kept_pair[r]
+ * of token u / k.  The dW GEMMs copy their x / phi operand rows by index straight into the
+ * operand tiles; the SwiGLU epilogue reads h by index.  Results are bit-identical to
+ * lrm_grouped_backward on the materialised buffers (same values, same order of arithmetic).
+ *   kept_pair [cap] int32, x [T,H], h [T*k,2I], phi [T*k,I] (dt); the rest as in
+ *   lrm_grouped_backward.  Errors as there.
+ */
+lrm_status lrm_grouped_backward_gather(const int32_t* seg_offsets, const int32_t* kept_pair, int32_t k,
+                                       const void* dy_c, const void* x, const void* h, const void* phi,
+                                       const void* w_gate_up, const void* w_down, int32_t E, int32_t H, int32_t I,
+                                       lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
+                                       void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
+                                       int32_t* dev_status, cudaStream_t stream);
 
 /*
  * Routing-weight gradient of the pairs.  The layer output is out_t = sum_j alpha_{t,j} y_{t,j}

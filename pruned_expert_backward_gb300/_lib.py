@@ -30,6 +30,8 @@ SIGNATURES = {
     "lrm_grouped_backward": (C.c_int, [_p, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, C.c_int, _i64, _p, _p,
                                        _p, _p, _p, _p, _sz, _i32, _p, _p]),
     "lrm_router_grad": (C.c_int, [_p, _p, _p, _i64, _i32, _i64, _p, _p]),
+    "lrm_grouped_backward_gather": (C.c_int, [_p, _p, _i32, _p, _p, _p, _p, _p, _p, _i32, _i32, _i32, C.c_int, _i64,
+                                              _p, _p, _p, _p, _p, _p, _sz, _i32, _p, _p]),
     "lrm_route": (C.c_int, [_p, _i64, _i32, _i32, C.c_int, _i32, _i32, _i32, _p, _p, _p, _p, _p, _p, _sz, _p, _p]),
     "lrm_swiglu_forward": (C.c_int, [_p, _i64, _i32, C.c_int, _p, _p, _p]),
     "lrm_score_norms": (C.c_int, [_p, _p, _p, _i64, _i32, _i32, C.c_int, _p, _p, _p]),

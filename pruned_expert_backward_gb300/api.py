@@ -165,19 +165,23 @@ def lrm_select(topk_idx, scores, quotas, E, cap=None, seg_offsets=None, kept_pai
     return seg_offsets, kept_pair, row_of_pair
 
 
-def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=None, phi_c=None):
+def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=None, phi_c=None, dy_only=False):
+    """dy_only: write only dy_c (the compaction-free variant; x_c, h_c, phi_c are returned as None)."""
     T, H = g.shape
     k, I = phi.shape[-2], phi.shape[-1]
     dev, dt = g.device, g.dtype
     rows = max(int(cap), 1)
     dy_c = torch.empty(rows, H, dtype=dt, device=dev) if dy_c is None else dy_c
-    x_c = torch.empty(rows, H, dtype=dt, device=dev) if x_c is None else x_c
-    h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
-    phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
+    if dy_only:
+        x_c = h_c = phi_c = None
+    else:
+        x_c = torch.empty(rows, H, dtype=dt, device=dev) if x_c is None else x_c
+        h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
+        phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
     _ok(L.load().lrm_compact(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(alpha, "alpha", torch.float32),
                              _cuda(g, "g"), _cuda(x, "x", dt), _cuda(h, "h", dt), _cuda(phi, "phi", dt), T, k, H, I,
-                             _dt(g), int(cap), _cuda(dy_c, "dy_c", dt), _cuda(x_c, "x_c", dt),
-                             _cuda(h_c, "h_c", dt), _cuda(phi_c, "phi_c", dt), _stream()), "lrm_compact")
+                             _dt(g), int(cap), _cuda(dy_c, "dy_c", dt), _opt(x_c, "x_c", dt),
+                             _opt(h_c, "h_c", dt), _opt(phi_c, "phi_c", dt), _stream()), "lrm_compact")
     return dy_c, x_c, h_c, phi_c
 
 
@@ -203,6 +207,31 @@ def lrm_grouped_backward(seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, 
         _cuda(dh_c, "dh_c", dt), _cuda(dx_c, "dx_c", dt), _opt(row_dot, "row_dot", torch.float32),
         _cuda(ws, "ws"), ws.numel(), int(flags),
         _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_grouped_backward")
+    return dw_gate_up, dw_down, dh_c, dx_c
+
+
+def lrm_grouped_backward_gather(seg_offsets, kept_pair, k, dy_c, x, h, phi, w_gate_up, w_down, cap,
+                                dw_gate_up=None, dw_down=None, dh_c=None, dx_c=None, ws=None,
+                                flags=L.LRM_GEMM_DEFAULT, dev_status=None, row_dot=None):
+    """Compaction-free grouped backward: x [T,H], h [T,k,2I], phi [T,k,I] read in place via kept_pair."""
+    E, H, I = w_down.shape
+    dev, dt = w_down.device, w_down.dtype
+    rows = max(int(cap), 1)
+    dw_gate_up = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev) if dw_gate_up is None else dw_gate_up
+    dw_down = torch.empty(E, H, I, dtype=torch.float32, device=dev) if dw_down is None else dw_down
+    dh_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if dh_c is None else dh_c
+    dx_c = torch.empty(rows, H, dtype=dt, device=dev) if dx_c is None else dx_c
+    if ws is None:
+        ws_rows = int(cap) if row_dot is not None else 0
+        ws = torch.empty(lrm_workspace_size(ws_rows, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
+    _ok(L.load().lrm_grouped_backward_gather(
+        _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(kept_pair, "kept_pair", torch.int32), int(k),
+        _cuda(dy_c, "dy_c", dt), _cuda(x, "x", dt), _cuda(h, "h", dt), _cuda(phi, "phi", dt),
+        _cuda(w_gate_up, "w_gate_up", dt), _cuda(w_down, "w_down", dt), E, H, I, _dt(w_down), int(cap),
+        _cuda(dw_gate_up, "dw_gate_up", torch.float32), _cuda(dw_down, "dw_down", torch.float32),
+        _cuda(dh_c, "dh_c", dt), _cuda(dx_c, "dx_c", dt), _opt(row_dot, "row_dot", torch.float32),
+        _cuda(ws, "ws"), ws.numel(), int(flags), _opt(dev_status, "dev_status", torch.int32), _stream()),
+        "lrm_grouped_backward_gather")
     return dw_gate_up, dw_down, dh_c, dx_c
 
 
@@ -233,9 +262,12 @@ class PrunedBackward:
     every pair (`dalpha`, fp32 [T*k]; 0 for dropped pairs)."""
 
     def __init__(self, T, k, E, H, I, dtype=torch.bfloat16, device="cuda", cap=None, flags=L.LRM_GEMM_DEFAULT,
-                 router_grad=False):
+                 router_grad=False, compaction="materialised"):
+        if compaction not in ("materialised", "gather"):
+            raise ValueError("compaction: 'materialised' (the pages' physical compaction) or 'gather'")
         self.T, self.k, self.E, self.H, self.I = T, k, E, H, I
         self.dtype, self.flags, self.router_grad = dtype, flags, router_grad
+        self.gather = compaction == "gather"
         self.cap = T * k if cap is None else int(cap)
         dev = torch.device(device)
         rows = max(self.cap, 1)
@@ -245,9 +277,10 @@ class PrunedBackward:
         self.kept_pair = torch.empty(rows, **i32)
         self.row_of_pair = torch.empty(max(T * k, 1), **i32)
         self.dy_c = torch.empty(rows, H, dtype=dtype, device=dev)
-        self.x_c = torch.empty(rows, H, dtype=dtype, device=dev)
-        self.h_c = torch.empty(rows, 2 * I, dtype=dtype, device=dev)
-        self.phi_c = torch.empty(rows, I, dtype=dtype, device=dev)
+        # the compaction-free variant keeps x, h, phi where they are
+        self.x_c = None if self.gather else torch.empty(rows, H, dtype=dtype, device=dev)
+        self.h_c = None if self.gather else torch.empty(rows, 2 * I, dtype=dtype, device=dev)
+        self.phi_c = None if self.gather else torch.empty(rows, I, dtype=dtype, device=dev)
         self.dh_c = torch.empty(rows, 2 * I, dtype=dtype, device=dev)
         self.dx_c = torch.empty(rows, H, dtype=dtype, device=dev)
         self.dw_gate_up = torch.empty(E, 2 * I, H, dtype=torch.float32, device=dev)
@@ -269,11 +302,18 @@ class PrunedBackward:
         lrm_select(inp["topk_idx"], self.scores, quotas, self.E, cap=self.cap, seg_offsets=self.seg_offsets,
                    kept_pair=self.kept_pair, row_of_pair=self.row_of_pair, ws=self.ws, dev_status=self.dev_status)
         lrm_compact(self.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], self.cap,
-                    dy_c=self.dy_c, x_c=self.x_c, h_c=self.h_c, phi_c=self.phi_c)
-        lrm_grouped_backward(self.seg_offsets, self.dy_c, self.x_c, self.h_c, self.phi_c, inp["w_gate_up"],
-                             inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
-                             dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
-                             dev_status=self.dev_status, row_dot=self.row_dot)
+                    dy_c=self.dy_c, x_c=self.x_c, h_c=self.h_c, phi_c=self.phi_c, dy_only=self.gather)
+        if self.gather:
+            lrm_grouped_backward_gather(self.seg_offsets, self.kept_pair, self.k, self.dy_c, inp["x"], inp["h"],
+                                        inp["phi"], inp["w_gate_up"], inp["w_down"], self.cap,
+                                        dw_gate_up=self.dw_gate_up, dw_down=self.dw_down, dh_c=self.dh_c,
+                                        dx_c=self.dx_c, ws=self.ws, flags=self.flags, dev_status=self.dev_status,
+                                        row_dot=self.row_dot)
+        else:
+            lrm_grouped_backward(self.seg_offsets, self.dy_c, self.x_c, self.h_c, self.phi_c, inp["w_gate_up"],
+                                 inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
+                                 dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
+                                 dev_status=self.dev_status, row_dot=self.row_dot)
         lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx)
         if self.router_grad:
             lrm_router_grad(self.row_of_pair, inp["alpha"], self.row_dot, self.T, self.k, self.cap,

@@ -210,8 +210,11 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
   if (st) return st;
   if ((st = check_dt(dt))) return st;
   if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
-  if (T > 0 && (!row_of_pair || !alpha || !g || !x || !h || !phi)) return LRM_ERR_INVALID_ARG;
-  if (cap > 0 && (!dy_c || !x_c || !h_c || !phi_c)) return LRM_ERR_INVALID_ARG;
+  // x_c, h_c, phi_c all NULL: the compaction-free variant (only dy_c is written)
+  const bool dy_only = !x_c && !h_c && !phi_c;
+  if (T > 0 && (!row_of_pair || !alpha || !g)) return LRM_ERR_INVALID_ARG;
+  if (T > 0 && !dy_only && (!x || !h || !phi)) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && (!dy_c || (!dy_only && (!x_c || !h_c || !phi_c)))) return LRM_ERR_INVALID_ARG;
   const void* ptrs[] = {g, x, h, phi, dy_c, x_c, h_c, phi_c};
   for (const void* p : ptrs)
     if (!al16(p)) return LRM_ERR_INVALID_ARG;
@@ -219,26 +222,38 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
   return after_launch();
 }
 
-lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
-                                const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E, int32_t H,
-                                int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
-                                void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
-                                int32_t* dev_status, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Shared by both grouped-backward entry points: validation, workspace carving, dispatch.
+lrm_status grouped_impl(GroupedArgs a, lrm_dtype dt, void* ws, size_t ws_bytes, int32_t flags,
+                        cudaStream_t stream) {
+  const int32_t E = a.E, H = a.H, I = a.I;
+  const int64_t cap = a.cap;
   lrm_status st = check_dims(0, 1, E, H, I);
   if (st) return st;
   if ((st = check_dt(dt))) return st;
   if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;
   if (flags != LRM_GEMM_DEFAULT && flags != LRM_GEMM_FORCE_SIMT) return LRM_ERR_INVALID_ARG;
-  if (!seg_offsets || !w_gate_up || !w_down || !dw_gate_up || !dw_down) return LRM_ERR_INVALID_ARG;
-  if (cap > 0 && (!dy_c || !x_c || !h_c || !phi_c || !dh_c || !dx_c)) return LRM_ERR_INVALID_ARG;
-  const void* ptrs[] = {dy_c, x_c, h_c, phi_c, w_gate_up, w_down, dw_gate_up, dw_down, dh_c, dx_c};
+  if (!a.seg_offsets || !a.w_gate_up || !a.w_down || !a.dw_gate_up || !a.dw_down) return LRM_ERR_INVALID_ARG;
+  const bool gather = a.kept_pair != nullptr;
+  if (cap > 0 && (!a.dy_c || !a.dh_c || !a.dx_c)) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && !gather && (!a.x_c || !a.h_c || !a.phi_c)) return LRM_ERR_INVALID_ARG;
+  if (cap > 0 && gather && (!a.x || !a.h || !a.phi || a.k < 1 || a.k > LRM_MAX_TOPK)) return LRM_ERR_INVALID_ARG;
+  const void* ptrs[] = {a.dy_c, a.x_c, a.h_c, a.phi_c, a.w_gate_up, a.w_down, a.dw_gate_up, a.dw_down, a.dh_c,
+                        a.dx_c, a.x, a.h, a.phi};
   for (const void* p : ptrs)
     if (!al16(p)) return LRM_ERR_INVALID_ARG;
-  if (row_dot && (reinterpret_cast<uintptr_t>(row_dot) & 3u)) return LRM_ERR_INVALID_ARG;
-  if (!ws || ws_bytes < grouped_ws_bytes(cap, E, I, row_dot != nullptr)) return LRM_ERR_WORKSPACE;
-  float* dot_part = row_dot ? reinterpret_cast<float*>(static_cast<char*>(ws) + up(gemm_ws_bytes(E))) : nullptr;
-  GroupedArgs a{seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, E, H, I, cap,
-                dw_gate_up, dw_down, dh_c, dx_c, dev_status, row_dot, dot_part};
+  if (a.row_dot && (reinterpret_cast<uintptr_t>(a.row_dot) & 3u)) return LRM_ERR_INVALID_ARG;
+  if (!ws || ws_bytes < grouped_ws_bytes(cap, E, I, a.row_dot != nullptr)) return LRM_ERR_WORKSPACE;
+  if (cap == 0) {  // no rows anywhere (seg_offsets[E] <= cap): every dW is exactly zero
+    if (cudaMemsetAsync(a.dw_gate_up, 0, sizeof(float) * (size_t)E * 2 * I * H, stream) != cudaSuccess ||
+        cudaMemsetAsync(a.dw_down, 0, sizeof(float) * (size_t)E * H * I, stream) != cudaSuccess)
+      return LRM_ERR_CUDA;
+    return LRM_OK;
+  }
+  a.dot_part = a.row_dot ? reinterpret_cast<float*>(static_cast<char*>(ws) + up(gemm_ws_bytes(E))) : nullptr;
   if (dt == LRM_BF16 && flags == LRM_GEMM_DEFAULT) {
     // workspace: tile tables and per-expert tensor maps at the start of ws
     GemmWs gw;
@@ -248,6 +263,32 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
   }
   launch_grouped_simt(a, dt, stream);
   return after_launch();
+}
+
+}  // namespace
+
+extern "C" {
+
+lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, const void* x_c, const void* h_c,
+                                const void* phi_c, const void* w_gate_up, const void* w_down, int32_t E, int32_t H,
+                                int32_t I, lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
+                                void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
+                                int32_t* dev_status, cudaStream_t stream) {
+  GroupedArgs a{seg_offsets, dy_c, x_c, h_c, phi_c, w_gate_up, w_down, E, H, I, cap, dw_gate_up, dw_down,
+                dh_c, dx_c, dev_status, row_dot, nullptr, nullptr, 0, nullptr, nullptr, nullptr};
+  return grouped_impl(a, dt, ws, ws_bytes, flags, stream);
+}
+
+lrm_status lrm_grouped_backward_gather(const int32_t* seg_offsets, const int32_t* kept_pair, int32_t k,
+                                       const void* dy_c, const void* x, const void* h, const void* phi,
+                                       const void* w_gate_up, const void* w_down, int32_t E, int32_t H, int32_t I,
+                                       lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
+                                       void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
+                                       int32_t* dev_status, cudaStream_t stream) {
+  if (cap > 0 && !kept_pair) return LRM_ERR_INVALID_ARG;
+  GroupedArgs a{seg_offsets, dy_c, nullptr, nullptr, nullptr, w_gate_up, w_down, E, H, I, cap, dw_gate_up,
+                dw_down, dh_c, dx_c, dev_status, row_dot, nullptr, kept_pair, k, x, h, phi};
+  return grouped_impl(a, dt, ws, ws_bytes, flags, stream);
 }
 
 lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,

@@ -51,7 +51,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   const T* xt = x + t * H;
   for (int v = tid; v < nvH; v += nt) {
     const uint4 gv = ld_stream16(gt + v * VN);
-    const uint4 xv = ld_stream16(xt + v * VN);
+    const uint4 xv = x_c != nullptr ? ld_stream16(xt + v * VN) : make_uint4(0, 0, 0, 0);
     float f[VN];
     unpack(gv, f);
     for (int j = 0; j < k; ++j) {
@@ -62,9 +62,10 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
 #pragma unroll
       for (int q = 0; q < VN; ++q) o[q] = a * f[q];
       st16(dy_c + r * H + v * VN, pack(o));
-      st16(x_c + r * H + v * VN, xv);
+      if (x_c != nullptr) st16(x_c + r * H + v * VN, xv);
     }
   }
+  if (h_c == nullptr) return;  // compaction-free variant: only the scaled gradient rows
 
   const int nv2 = 2 * I / VN;
   const T* ht = h + t * k * (int64_t)(2 * I);

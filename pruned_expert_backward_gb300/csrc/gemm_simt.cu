@@ -59,7 +59,9 @@ template <typename T, int EPI>
 __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ seg, int E,
                                                   const T* __restrict__ A, const T* __restrict__ B, int K, int N,
                                                   const T* __restrict__ h_c, T* __restrict__ out,
-                                                  float* __restrict__ dot_part, int n_part) {
+                                                  float* __restrict__ dot_part, int n_part,
+                                                  const int32_t* __restrict__ h_rows) {
+  // h_rows (compaction-free variant): the gate/up row of output row r is h_c[h_rows[r]]
   __shared__ int s_prefix[LRM_MAX_EXPERTS + 1];
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
@@ -116,8 +118,9 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
       if (n >= N) continue;
       if (EPI == EPI_SWIGLU) {
         // N = I here; h_c row is [gate (I) ; up (I)]
-        const float gate = to_f(h_c[(int64_t)r * 2 * N + n]);
-        const float up = to_f(h_c[(int64_t)r * 2 * N + N + n]);
+        const int64_t hr = h_rows ? (int64_t)h_rows[r] : (int64_t)r;
+        const float gate = to_f(h_c[hr * 2 * N + n]);
+        const float up = to_f(h_c[hr * 2 * N + N + n]);
         const float sg = 1.f / (1.f + expf(-gate));
         const float dphi = acc[i][j];
         const float du = dphi * gate * sg;
@@ -141,10 +144,12 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
   }
 }
 
-// C_e[m, n] = sum_{r in segment e} A[r, m] * B[r, n]; A [rows, M], B [rows, N] row-major.
+// C_e[m, n] = sum_{r in segment e} A[r, m] * B[r', n]; A [rows, M], B [*, N] row-major, where
+// r' = r, or (compaction-free variant) r' = b_rows[r] / b_div (b_div > 0) or b_rows[r].
 template <typename T>
 __global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ seg, const T* __restrict__ A,
-                                                  const T* __restrict__ B, int M, int N, float* __restrict__ C) {
+                                                  const T* __restrict__ B, int M, int N, float* __restrict__ C,
+                                                  const int32_t* __restrict__ b_rows, int b_div) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
   const int e = blockIdx.z;
@@ -156,11 +161,13 @@ __global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ se
     {
       const int kk = threadIdx.x / 16, q4 = (threadIdx.x % 16) * 4;
       const int r = k0 + kk;
+      int64_t rb = r;
+      if (b_rows != nullptr && r < r1) rb = b_div > 0 ? b_rows[r] / b_div : b_rows[r];
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int m = m0 + q4 + q, n = n0 + q4 + q;
         As[kk][q4 + q] = (r < r1 && m < M) ? to_f(A[(int64_t)r * M + m]) : 0.f;
-        Bs[kk][q4 + q] = (r < r1 && n < N) ? to_f(B[(int64_t)r * N + n]) : 0.f;
+        Bs[kk][q4 + q] = (r < r1 && n < N) ? to_f(B[rb * N + n]) : 0.f;
       }
     }
     __syncthreads();
@@ -197,28 +204,31 @@ void run_all(const GroupedArgs& a, cudaStream_t s) {
   // Upper bound on M tiles: every expert adds at most one partial tile.
   const int64_t mtiles = (a.cap + BM - 1) / BM + E;
   const T* dy = (const T*)a.dy_c;
-  const T* xc = (const T*)a.x_c;
-  const T* hc = (const T*)a.h_c;
-  const T* pc = (const T*)a.phi_c;
+  const bool gather = a.kept_pair != nullptr;  // compaction-free: x / h / phi rows read by index
+  const T* xc = (const T*)(gather ? a.x : a.x_c);
+  const T* hc = (const T*)(gather ? a.h : a.h_c);
+  const T* pc = (const T*)(gather ? a.phi : a.phi_c);
   T* dh = (T*)a.dh_c;
   T* dx = (T*)a.dx_c;
   if (mtiles > 0) {
     // dphi + SwiGLU backward: [R_e, H] x [H, I]
     const int n_part = (I + BN - 1) / BN;
     varm_kernel<T, EPI_SWIGLU><<<dim3((unsigned)mtiles, n_part), NT, 0, s>>>(
-        a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh, a.row_dot ? a.dot_part : nullptr, n_part);
+        a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh, a.row_dot ? a.dot_part : nullptr, n_part,
+        a.kept_pair);
     if (a.row_dot != nullptr) launch_row_dot(a.dot_part, n_part, a.seg_offsets, E, a.cap, a.row_dot, s);
   }
   // dW_down[e] = dy_c^T phi_c : [H, I]
   vark_kernel<T><<<dim3((I + BN - 1) / BN, (H + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, dy, pc, H, I,
-                                                                              a.dw_down);
+                                                                              a.dw_down, a.kept_pair, 0);
   // dW_gate_up[e] = dh_c^T x_c : [2I, H]
   vark_kernel<T><<<dim3((H + BN - 1) / BN, (2 * I + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, (const T*)dh, xc,
-                                                                                  2 * I, H, a.dw_gate_up);
+                                                                                  2 * I, H, a.dw_gate_up,
+                                                                                  a.kept_pair, a.k);
   if (mtiles > 0) {
     // dx_c = dh_c W_gate_up[e] : [R_e, 2I] x [2I, H]
     varm_kernel<T, EPI_STORE><<<dim3((unsigned)mtiles, (H + BN - 1) / BN), NT, 0, s>>>(
-        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx, nullptr, 0);
+        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx, nullptr, 0, nullptr);
   }
 }
 

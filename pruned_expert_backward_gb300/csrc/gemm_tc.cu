@@ -55,7 +55,11 @@ constexpr int kABytes = kBM * kBK * 2;            // 16 KB: this CTA's 128 rows 
 constexpr int kBHalfBytes = (kBN / 2) * kBK * 2;  // 16 KB: this CTA's 128 columns of B
 constexpr int kStageBytes = kABytes + kBHalfBytes;
 constexpr int kEpiWarps = 8;  // two per TMEM lane quarter, each taking half of the columns
-constexpr int kThreads = 64 + 32 * kEpiWarps;
+// Gathering B rows (compaction-free variant), warp 0 and these extra warps copy them: one warp
+// alone cannot keep enough copies in flight.  Other launches leave the extra warps idle.
+constexpr int kGatherExtraWarps = 2;
+constexpr int kGatherWarps = 1 + kGatherExtraWarps;
+constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kGatherExtraWarps;
 // Epilogue staging per epilogue warp: a 32 x 32 fp32 block with rows padded to 33 floats
 // (scalar shared accesses are conflict-free both row-per-thread and row-contiguous).
 constexpr int kVmLd = 33;
@@ -67,6 +71,11 @@ constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
 enum Kind { VM_SWIGLU = 0, VM_STORE = 1, VK = 2 };
+
+template <bool B>
+struct BoolTag {
+  static constexpr bool value = B;
+};
 
 struct TcParams {
   int kind;
@@ -82,6 +91,13 @@ struct TcParams {
   const CUtensorMap* maps_b;  //     expert's segment end (TMA zero-fills the rows beyond it)
   float* dot_part;            // VM_SWIGLU, optional: [rows][n_part] parts of dphi . phi (one per
   int n_part;                 //     128 output columns), summed in order by the reduce kernel
+  // Gather mode (kept_pair non-null; the compaction-free variant): compacted row r stands for
+  // pair u = kept_pair[r].  VM_SWIGLU reads gate/up from gsrc = h [P, 2I] at row u; VK gathers
+  // its B operand rows from gsrc (phi at row u, or x at row u / gk when gk > 0) with cp.async.
+  const int32_t* kept_pair;
+  const __nv_bfloat16* gsrc;
+  int gk;   // VK: > 0 when the gathered rows are tokens (u / gk)
+  int gld;  // elements per row of gsrc
 };
 
 // ---------------------------------------------------------------- PTX wrappers -------
@@ -113,14 +129,26 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+__device__ __forceinline__ bool mbar_try_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Bounded wait.  Returns false (and raises the abort flag) when the barrier does not
 // complete within kWaitNs, or when another role of the CTA has already aborted.  The common
 // case (already complete) stays inline; the polling loop is out of line.
 __device__ __noinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                            int32_t* status, bool honour_abort, uint64_t limit_ns = kWaitNs) {
+                                            int32_t* status, bool honour_abort, uint64_t limit_ns = kWaitNs,
+                                            bool cluster_acquire = false) {
   const uint64_t t0 = globaltimer();
   for (uint32_t it = 1; it < (1u << 30); ++it) {
-    if (mbar_try(bar, parity)) return true;
+    if (cluster_acquire ? mbar_try_cluster(bar, parity) : mbar_try(bar, parity)) return true;
     if ((it & 255u) == 0) {
       if (honour_abort && *abort_flag) return false;
       if (globaltimer() - t0 > limit_ns) break;
@@ -134,6 +162,13 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, volatil
                                           bool honour_abort = true) {
   if (mbar_try(bar, parity)) return true;
   return mbar_wait_slow(bar, parity, abort_flag, status, honour_abort);
+}
+// The same with cluster-scope acquire: the waiter then sees what the other CTA of the pair wrote
+// before its release-arrive (shared-memory operands copied by threads, not by TMA).
+__device__ __forceinline__ bool mbar_wait_cl(uint32_t bar, uint32_t parity, volatile int* abort_flag,
+                                             int32_t* status) {
+  if (mbar_try_cluster(bar, parity)) return true;
+  return mbar_wait_slow(bar, parity, abort_flag, status, true, kWaitNs, true);
 }
 // Cluster helpers.  CTAs run in pairs (a cluster of two); the even CTA is the MMA leader.
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -172,6 +207,25 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "%3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
       : "memory");
+}
+// 16-byte cp.async into shared memory; src_bytes < 16 zero-fills the rest (0: nothing is read).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
+}
+// The mbarrier receives one arrival once all of this thread's earlier cp.async have completed
+// (the barrier's expected count includes it; the thread does not wait).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// Generic-proxy writes to shared memory become visible to the async proxy (tensor core reads).
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// Arrive on an mbarrier of either CTA of the pair, ordering this thread's earlier writes before it
+// for a waiter anywhere in the cluster.
+__device__ __forceinline__ void mbar_arrive_release_cluster(uint32_t cbar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cbar) : "memory");
 }
 // TMA tensor store from this CTA's shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int c0, int c1, int c2) {
@@ -302,8 +356,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   constexpr int S = kStages;
   uint8_t* epi = smem + epi_offset();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_offset());
-  // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 2 * S + 5);
+  // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain, gathered[S]
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -313,10 +367,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t full0 = smem_u32(bars), empty0 = smem_u32(bars + S);
   const uint32_t accf0 = smem_u32(bars + 2 * S), acce0 = smem_u32(bars + 2 * S + 2);
   const uint32_t drain = smem_u32(bars + 2 * S + 4);
+  const uint32_t gath0 = smem_u32(bars + 2 * S + 5);  // this CTA's gathered B rows of a stage landed
 
+  const bool gather_b = p.kind == VK && p.kept_pair != nullptr;  // B rows gathered by threads
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
-      mbar_init(full0 + 8 * s, 2);   // leader's: both producers arrive with their byte counts
+      // leader's: both producers arrive with their byte counts (and, gathering, the other CTA
+      // once more when its copies of the stage have landed)
+      mbar_init(full0 + 8 * s, gather_b ? 3 : 2);
+      mbar_init(gath0 + 8 * s, 32 * kGatherWarps);  // gathering: every copying lane's copies
       mbar_init(empty0 + 8 * s, 1);  // the leader's MMA commit, multicast to the pair
     }
     mbar_init(accf0, 1);
@@ -337,7 +396,102 @@ __global__ void __launch_bounds__(kThreads, 1)
   volatile int* abortv = abort_flag;
   const uint32_t full_lead = cluster_addr(full0, 0), acce_lead = cluster_addr(acce0, 0);
 
-  if (warp == 0) {
+  const int first_extra = 2 + kEpiWarps;  // warps first_extra.. are the extra gather warps
+  if (gather_b && (warp == 0 || warp >= first_extra)) {
+    // ------------------------------------------------ producer, B rows gathered --------
+    // A (the compacted rows) still comes by TMA from warp 0's lane 0.  The B rows of a K slice
+    // are pairs (or their tokens) named by kept_pair: the gather warps copy this CTA's 128
+    // columns of the slice's 64 rows (row pairs split round-robin between them) with 16-byte
+    // cp.async straight into the 128-byte-swizzled MN-major layout a TMA box would produce
+    // (rows past the segment and columns past N are zero-filled).
+    // Each lane's copies of a stage arrive on gathered[s] when they land; the lanes never wait.
+    // The walk over (tile, K slice) is flat, and the next slice's row indices are loaded one
+    // step ahead (across tiles too), so the copies never wait on an index load.
+    const int gw = warp == 0 ? 0 : warp - first_extra + 1;  // this warp's share of the rows
+    uint32_t it = 0, st = 0, sph = 0;
+    bool ok = true;
+    int last_e = -1;
+    // pairs named by kept_pair for K rows r0 + lane and r0 + 32 + lane of a slice (-1 past the segment)
+    auto load_idx = [&](const Tile& dd, int kbb, int& u0, int& u1) {
+      const int r0 = dd.row0 + kbb * kBK;
+      u0 = r0 + lane < dd.row_end ? __ldg(p.kept_pair + r0 + lane) : -1;
+      u1 = r0 + 32 + lane < dd.row_end ? __ldg(p.kept_pair + r0 + 32 + lane) : -1;
+    };
+    int t = pair, kb = 0;
+    Tile d{};
+    bool have = false;
+    for (; t < n_tiles; t += n_pairs) {
+      d = decode(p, t, rank);
+      if (d.k_iters > 0) { have = true; break; }
+    }
+    int cu0 = -1, cu1 = -1;
+    if (have) load_idx(d, 0, cu0, cu1);
+    while (have) {
+      // the slice after this one, and its indices (used next step)
+      int tn = t, kbn = kb + 1;
+      Tile dn = d;
+      bool haven = true;
+      if (kbn >= d.k_iters) {
+        kbn = 0;
+        haven = false;
+        for (tn = t + n_pairs; tn < n_tiles; tn += n_pairs) {
+          dn = decode(p, tn, rank);
+          if (dn.k_iters > 0) { haven = true; break; }
+        }
+      }
+      int nu0 = -1, nu1 = -1;
+      if (haven) load_idx(dn, kbn, nu0, nu1);
+
+      const CUtensorMap* ma = p.maps_a + d.e;
+      if (gw == 0 && lane == 0 && d.e != last_e) tensormap_acquire(ma);
+      last_e = d.e;
+      const uint32_t s = st, ph = sph;
+      if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
+      bool w = true;
+      if (lane == 0) w = mbar_wait(empty0 + 8 * s, ph ^ 1u, abortv, p.status);
+      if (!__shfl_sync(0xffffffffu, w ? 1 : 0, 0)) { ok = false; break; }
+      const uint32_t a_dst = smem_u32(smem + s * kStageBytes), b_dst = a_dst + kABytes;
+      const uint32_t fb = full_lead + 8 * s;
+      const int r0 = d.row0 + kb * kBK;
+      if (gw == 0 && lane == 0) {
+        mbar_expect_tx_cluster(fb, d.has_rows ? kABytes : 0);
+        if (d.has_rows) {
+          tma_load_2d_pair(a_dst, ma, d.m0, r0, fb);
+          tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r0, fb);
+        }
+      }
+      // source rows (pairs, or their tokens) of K rows lane and lane + 32
+      const int sr0 = cu0 < 0 ? -1 : (p.gk > 0 ? cu0 / p.gk : cu0);
+      const int sr1 = cu1 < 0 ? -1 : (p.gk > 0 ? cu1 / p.gk : cu1);
+      // each instruction copies two rows' 256 contiguous bytes: half-warp hi = lane >> 4 takes
+      // row 2j + hi, its lanes the 16 chunks (MN block b = chunk >> 3, 16-byte chunk c = chunk & 7)
+      const int nb = d.n0 + rank * (kBN / 2);
+      const int hi = lane >> 4, b = (lane >> 3) & 1, c = lane & 7;
+      const int col = nb + b * 64 + c * 8;
+      const bool col_live = col < p.N;
+      for (int j = gw; j < 32; j += kGatherWarps) {
+        const int l = 2 * j + hi;  // K row of the slice
+        const int sr = __shfl_sync(0xffffffffu, l < 32 ? sr0 : sr1, l & 31);
+        const bool live = col_live && sr >= 0;
+        cp_async16(b_dst + b * 8192 + l * 128 + ((c ^ (l & 7)) << 4),
+                   live ? p.gsrc + (int64_t)sr * p.gld + col : p.gsrc, live ? 16u : 0u);
+      }
+      cp_async_arrive_noinc(gath0 + 8 * s);
+      ++it;
+      t = tn;
+      kb = kbn;
+      d = dn;
+      have = haven;
+      cu0 = nu0;
+      cu1 = nu1;
+    }
+    cp_async_wait_all();  // no copy may outlive the CTA (after an abort too)
+    if (gw == 0 && lane == 0) {
+      // drain: every stage this warp filled has been consumed
+      const uint32_t first = it > (uint32_t)S ? it - S : 0u;
+      for (uint32_t i = first; i < it; ++i) mbar_wait(empty0 + 8 * (i % S), (i / S) & 1u, abortv, p.status, false);
+    }
+  } else if (warp == 0) {
     // ------------------------------------------------------------ TMA producer -------
     // Both CTAs load their own 128 rows of A and their own 128 columns of B; the loads
     // complete on the leader's full barrier, which the leader's MMA waits on.
@@ -397,36 +551,74 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t adesc0 = p.kind == VK ? smem_desc(a0, 8192, 1024) : smem_desc(a0, 16, 1024);
       const uint64_t bdesc0 = smem_desc(b0, 8192, 1024);
       const uint64_t a_kstep = p.kind == VK ? (2048 >> 4) : (32 >> 4), b_kstep = 2048 >> 4;
+      // the issue loop, compiled once per kind of B delivery (the loop is on the critical path)
+      auto issue = [&](auto gather_tag) {
+        constexpr bool G = decltype(gather_tag)::value;
+        uint32_t st = 0, sph = 0;
+        int lt = 0;
+        bool ok = true;
+        for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+          const Tile d = decode(p, t, 0);
+          const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
+          if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
+          tc_fence_after();
+          const uint32_t tmem_d = tmem_base + acc * kBN;
+          for (int kb = 0; kb < d.k_iters; ++kb) {
+            const uint32_t s = st, ph = sph;
+            if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
+            if (!(G ? mbar_wait_cl(full0 + 8 * s, ph, abortv, p.status)
+                    : mbar_wait(full0 + 8 * s, ph, abortv, p.status))) {
+              ok = false;
+              break;
+            }
+            if (G) {
+              // this CTA's copied B rows have landed; make them visible to the tensor core (the
+              // other CTA's were fenced by its relay before it arrived on full)
+              if (!mbar_wait(gath0 + 8 * s, ph, abortv, p.status)) {
+                ok = false;
+                break;
+              }
+              fence_proxy_async_smem();
+            }
+            tc_fence_after();
+            const uint64_t soff = (uint64_t)((s * kStageBytes) >> 4);
+#pragma unroll
+            for (int kk = 0; kk < kBK / 16; ++kk)
+              mma_bf16(tmem_d, adesc0 + soff + kk * a_kstep, bdesc0 + soff + kk * b_kstep, idesc,
+                       (kb | kk) != 0 ? 1u : 0u);
+            mma_commit_pair(empty0 + 8 * s);
+          }
+          if (!ok) break;
+          mma_commit_pair(accf0 + 8 * acc);
+        }
+      };
+      if (gather_b) issue(BoolTag<true>{});
+      else issue(BoolTag<false>{});
+      mma_commit_pair(drain);
+    }
+    if (!leader && gather_b && lane == 0) {
+      // relay: once this CTA's copies of a stage have landed, fence them for the async proxy and
+      // release them to the leader's MMA through its full barrier
       uint32_t st = 0, sph = 0;
-      int lt = 0;
       bool ok = true;
-      for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
-        const Tile d = decode(p, t, 0);
-        const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
-        if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
-        tc_fence_after();
-        const uint32_t tmem_d = tmem_base + acc * kBN;
+      for (int t = pair; t < n_tiles && ok; t += n_pairs) {
+        const Tile d = decode(p, t, rank);
         for (int kb = 0; kb < d.k_iters; ++kb) {
           const uint32_t s = st, ph = sph;
           if (++st == (uint32_t)S) { st = 0; sph ^= 1u; }
-          if (!mbar_wait(full0 + 8 * s, ph, abortv, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint64_t soff = (uint64_t)((s * kStageBytes) >> 4);
-#pragma unroll
-          for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_bf16(tmem_d, adesc0 + soff + kk * a_kstep, bdesc0 + soff + kk * b_kstep, idesc,
-                     (kb | kk) != 0 ? 1u : 0u);
-          mma_commit_pair(empty0 + 8 * s);
+          if (!mbar_wait(gath0 + 8 * s, ph, abortv, p.status)) {
+            ok = false;
+            break;
+          }
+          fence_proxy_async_smem();
+          mbar_arrive_release_cluster(full_lead + 8 * s);
         }
-        if (!ok) break;
-        mma_commit_pair(accf0 + 8 * acc);
       }
-      mma_commit_pair(drain);
     }
     __syncwarp();
     // drain: all MMAs writing this CTA's TMEM complete before it is released
     mbar_wait(drain, 0, abortv, p.status, false);
-  } else {
+  } else if (warp >= 2 && warp < first_extra) {
     // ------------------------------------------------------------ epilogue -----------
     // Warp w may read TMEM lanes 32*(w%4) .. +31 (tile rows q*32 .. q*32+31); the two warps
     // of a quarter split the eight 32-column chunks.  Each chunk is read row-per-thread
@@ -486,7 +678,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int i = 0; i < 4; ++i) {
               const int rr = i * 8 + sub;
               if (rr < nrows && col < I) {
-                const __nv_bfloat16* hrow = p.h_c + (int64_t)(row_base + rr) * 2 * I;
+                // gate/up row: the compacted row, or (compaction-free) the pair's row of h
+                const __nv_bfloat16* hrow =
+                    p.kept_pair ? p.gsrc + (int64_t)__ldg(p.kept_pair + row_base + rr) * 2 * I
+                                : p.h_c + (int64_t)(row_base + rr) * 2 * I;
                 gv[i] = ldg16(hrow + col);
                 uv[i] = ldg16(hrow + I + col);
               }
@@ -683,7 +878,7 @@ bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-size_t smem_bytes() { return 1024 + bar_offset() + (2 * kStages + 5) * 8 + 8; }
+size_t smem_bytes() { return 1024 + bar_offset() + (3 * kStages + 5) * 8 + 8; }
 
 int sm_count() {
   static int n = 0;
@@ -721,7 +916,8 @@ lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  cfg.blockDim = dim3(kThreads);
+  // the extra gather warps are launched only where B rows are gathered
+  cfg.blockDim = dim3(p.kind == VK && p.kept_pair != nullptr ? kThreads : kThreads - 32 * kGatherExtraWarps);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
@@ -753,8 +949,12 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   int32_t* plan = ws.plan;  // [2E+1] tile tables
   CUtensorMap* maps = static_cast<CUtensorMap*>(ws.maps);
   MapTemplates tpl;
-  if (!make_map_2d(&tpl.t[0], g.dy_c, rows, H, 64) || !make_map_2d(&tpl.t[1], g.phi_c, rows, I, 64) ||
-      !make_map_2d(&tpl.t[2], g.dh_c, rows, 2 * I, 64) || !make_map_2d(&tpl.t[3], g.x_c, rows, H, 64))
+  const bool gather = g.kept_pair != nullptr;  // compaction-free: phi / x rows gathered by index
+  // (gathering, the B templates are never used; they are encoded over dy_c only to stay valid)
+  if (!make_map_2d(&tpl.t[0], g.dy_c, rows, H, 64) ||
+      !make_map_2d(&tpl.t[1], gather ? g.dy_c : g.phi_c, rows, I, 64) ||
+      !make_map_2d(&tpl.t[2], g.dh_c, rows, 2 * I, 64) ||
+      !make_map_2d(&tpl.t[3], gather ? g.dy_c : g.x_c, rows, H, 64))
     return LRM_ERR_CUDA;
   tc_plan_kernel<<<1, 1024, 0, s>>>(g.seg_offsets, E, plan, maps, tpl);
   if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
@@ -764,13 +964,16 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   lrm_status st;
   // dphi = dy_c W_down[e], SwiGLU backward fused -> dh_c
   if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !make_map_3d(&mB, g.w_down, E, H, I)) return LRM_ERR_CUDA;
+  using B16 = const __nv_bfloat16*;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
-             (const __nv_bfloat16*)g.h_c, g.status, nullptr, nullptr, g.dot_part, (I + 127) / 128};
+             (B16)g.h_c, g.status, nullptr, nullptr, g.dot_part, (I + 127) / 128,
+             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I};
   if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   if (g.row_dot != nullptr) launch_row_dot(g.dot_part, p.n_part, g.seg_offsets, E, g.cap, g.row_dot, s);
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
-               nullptr, g.status, maps + 0 * E, maps + 1 * E};
+               nullptr, g.status, maps + 0 * E, maps + 1 * E, nullptr, 0,
+               g.kept_pair, gather ? (B16)g.phi : nullptr, 0, I};
   mA = tpl.t[0];
   mB = tpl.t[1];
   CUtensorMap mC;
@@ -778,7 +981,8 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
   p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
-               g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E};
+               g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E, nullptr, 0,
+               g.kept_pair, gather ? (B16)g.x : nullptr, g.k, H};
   mA = tpl.t[2];
   mB = tpl.t[3];
   if (!make_map_out3d(&mC, g.dw_gate_up, E, 2 * I, H)) return LRM_ERR_CUDA;

@@ -77,6 +77,11 @@ struct GroupedArgs {
   int32_t* status;
   float* row_dot;   // optional [cap]: dphi . phi per retained row
   float* dot_part;  // scratch for row_dot: [cap][dot_parts_max(I)]
+  // Compaction-free variant (kept_pair non-null): x_c, h_c, phi_c are not used; their rows are
+  // read from x [T,H] (token u / k), h [P,2I] and phi [P,I] (pair u = kept_pair[r]).
+  const int32_t* kept_pair;
+  int32_t k;
+  const void *x, *h, *phi;
 };
 
 // Parts of the dphi . phi row sums: one per 128 output columns (tensor-core path) or per 64

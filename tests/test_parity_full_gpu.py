@@ -157,3 +157,26 @@ def test_full_size_router_grad(name):
         want[sel] = oracle.router_grad(np.zeros(len(sel), np.int64), np.zeros((len(sel), 1), np.int64),
                                        g[sel], phi[sel].astype(np.float64), wd)
     assert rel_fro(dalpha[pairs], want) <= TOL[wl.dtype], (name, rel_fro(dalpha[pairs], want))
+
+
+@pytest.mark.parametrize("name", ["qwen3_t8k_d20", "qwen3_t64k_zipf15_cap"])
+def test_full_size_compaction_free_bit_identical(name):
+    """At full size, in the launch configuration bench.py times: the compaction-free variant's
+    outputs equal the materialised path's bit for bit."""
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.WORKLOADS[name]
+    inp = W.generate(wl, "cuda", seed=0)
+    _, q = gpu_quotas(inp, wl)
+    res = []
+    for mode in ("materialised", "gather"):
+        pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, compaction=mode)
+        pb.run(inp, q)
+        torch.cuda.synchronize()
+        assert int(pb.dev_status.item()) == 0
+        res.append(pb)
+        del pb
+    a, b = res
+    R = int(a.seg_offsets[-1])
+    for n in ("dw_gate_up", "dw_down", "dx"):
+        assert torch.equal(getattr(a, n), getattr(b, n)), n
+    assert torch.equal(a.dh_c[:R], b.dh_c[:R]) and torch.equal(a.dx_c[:R], b.dx_c[:R])

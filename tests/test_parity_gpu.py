@@ -316,3 +316,58 @@ def test_ablation_scores_and_selection(mode):
     assert np.array_equal(to_np(seg), oseg)
     assert np.array_equal(to_np(kept)[: int(oseg[-1])], okept)
     assert np.array_equal(to_np(rop), orop)
+
+
+GATHER_CASES = SMALL + [W.small_workload("gather_i136_k6", 1536, 256, 136, 24, 6, quota=("ratio", 7, 10))]
+
+
+@pytest.mark.parametrize("wl", GATHER_CASES, ids=lambda w: w.name)
+def test_compaction_free_variant_is_bit_identical(wl):
+    """The gather variant reads x / h / phi rows in place; every output must equal the
+    materialised path's bit for bit (same values, same order of arithmetic), which the oracle
+    checks above."""
+    import pruned_expert_backward_gb300 as lrm
+    from helpers import gpu_quotas
+    inp = W.generate(wl, "cuda", seed=6)
+    loads, q = gpu_quotas(inp, wl)
+    for flags in GEMM_MODES[wl.dtype]:
+        outs = []
+        for mode in ("materialised", "gather"):
+            pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, flags=flags,
+                                    router_grad=True, compaction=mode)
+            pb.run(inp, q)
+            torch.cuda.synchronize()
+            assert int(pb.dev_status.item()) == 0, mode
+            outs.append(pb)
+        a, b = outs
+        R = int(a.seg_offsets[-1])
+        assert torch.equal(a.seg_offsets, b.seg_offsets)
+        for name in ("dw_gate_up", "dw_down", "dx", "dalpha"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), (name, flags)
+        for name in ("dy_c", "dh_c", "dx_c", "row_dot"):
+            assert torch.equal(getattr(a, name)[:R], getattr(b, name)[:R]), (name, flags)
+    full_check(wl, inp, loads, q, a)
+
+
+def test_compaction_free_edges():
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.small_workload("gather_edges", 400, 256, 128, 8, 2)
+    inp = W.generate(wl, "cuda", seed=7)
+    for flags in GEMM_MODES["bf16"]:
+        for quotas in (np.zeros(8, np.int32), np.full(8, 10 ** 6, np.int32)):
+            q = torch.as_tensor(quotas, device="cuda")
+            res = []
+            for mode in ("materialised", "gather"):
+                pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, flags=flags, compaction=mode)
+                pb.run(inp, q)
+                torch.cuda.synchronize()
+                assert int(pb.dev_status.item()) == 0
+                res.append(pb)
+            assert torch.equal(res[0].dw_down, res[1].dw_down) and torch.equal(res[0].dw_gate_up, res[1].dw_gate_up)
+            assert torch.equal(res[0].dx, res[1].dx)
+        # cap = 0: nothing can be kept, every dW is exactly zero
+        pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, flags=flags, compaction="gather", cap=0)
+        pb.run(inp, torch.zeros(8, dtype=torch.int32, device="cuda"))
+        torch.cuda.synchronize()
+        assert int(pb.dev_status.item()) == 0
+        assert torch.all(pb.dw_down == 0) and torch.all(pb.dw_gate_up == 0) and torch.all(pb.dx == 0)
