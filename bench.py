@@ -444,7 +444,7 @@ def next_rows(args, wl, inp, quotas, flags, dev, stream, ms_step, pk):
     # also emits ||phi||^2, and the score from those norms (phi not re-read)
     kind, num, den, cap, expl = W.quota_policy(wl)
     ex = None if expl is None else torch.tensor(expl, dtype=torch.int32, device=dev)
-    ws = torch.empty(64, dtype=torch.uint8, device=dev)
+    ws = torch.empty(4 * (wl.E + 1), dtype=torch.uint8, device=dev)
     r_out = [torch.empty(wl.T, wl.k, dtype=torch.int32, device=dev),
              torch.empty(wl.T, wl.k, dtype=torch.float32, device=dev),
              torch.empty(wl.E, dtype=torch.int32, device=dev), torch.empty(wl.E, dtype=torch.int32, device=dev)]

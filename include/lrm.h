@@ -252,7 +252,7 @@ lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t 
  *   descending order, ties to the lower expert id; alpha [T*k] fp32: softmax over those k logits;
  *   loads [E], quotas [E] int32 exactly as lrm_plan_quotas writes them for this routing.
  *   kind/num/den/cap/explicit_quotas as in lrm_plan_quotas.
- *   ws: any 4-byte-aligned device scratch of >= 4 bytes (a buffer of lrm_workspace_size bytes does).
+ *   ws: 4-byte-aligned device scratch of >= 4 * (E + 1) bytes (a buffer of lrm_workspace_size bytes does).
  * A non-finite logit is never chosen ahead of a finite one and sets LRM_ERR_NONFINITE in
  * dev_status.  Integer results are deterministic.  Errors: LRM_ERR_INVALID_ARG, LRM_ERR_SHAPE
  * (also k > E), LRM_ERR_WORKSPACE, LRM_ERR_CUDA.

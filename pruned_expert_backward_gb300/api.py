@@ -111,7 +111,7 @@ def lrm_route(logits, k, kind, num=0, den=1, cap=0, explicit=None, topk_idx=None
     alpha = torch.empty(T, k, dtype=torch.float32, device=dev) if alpha is None else alpha
     loads = torch.empty(E, **i32) if loads is None else loads
     quotas = torch.empty(E, **i32) if quotas is None else quotas
-    ws = torch.empty(64, dtype=torch.uint8, device=dev) if ws is None else ws
+    ws = torch.empty(4 * (E + 1), dtype=torch.uint8, device=dev) if ws is None else ws
     kinds = {"ratio": L.LRM_QUOTA_RATIO, "cap": L.LRM_QUOTA_CAP, "explicit": L.LRM_QUOTA_EXPLICIT}
     _ok(L.load().lrm_route(_cuda(logits, "logits", torch.float32), T, E, k, kinds[kind], num, den, cap,
                            _opt(explicit, "explicit", torch.int32), _cuda(topk_idx, "topk_idx", torch.int32),

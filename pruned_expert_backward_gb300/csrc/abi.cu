@@ -148,7 +148,7 @@ lrm_status lrm_route(const float* logits, int64_t T, int32_t E, int32_t k, lrm_q
   } else {
     return LRM_ERR_INVALID_ARG;
   }
-  if (!ws || ws_bytes < sizeof(uint32_t) || (reinterpret_cast<uintptr_t>(ws) & 3u)) return LRM_ERR_WORKSPACE;
+  if (!ws || ws_bytes < sizeof(uint32_t) * (E + 1) || (reinterpret_cast<uintptr_t>(ws) & 3u)) return LRM_ERR_WORKSPACE;
   return launch_route(logits, T, E, k, (int)kind, num, den, cap, explicit_quotas, topk_idx, alpha, loads, quotas,
                       static_cast<uint32_t*>(ws), dev_status, stream);
 }

@@ -7,7 +7,8 @@
 //   is decided.  One warp per token keeps the token's logits in registers (lane l holds experts
 //   l, l+32, ...), picks the k largest by repeated warp arg-max (ties to the lower expert id) and
 //   takes the softmax over them; a CTA counts its tokens' experts in shared memory and adds the
-//   counts to `loads`; the CTA that finishes last applies the quota rule.
+//   counts to accumulators in the workspace; the CTA that finishes last copies them to `loads`
+//   and applies the quota rule.  A few CTAs per SM walk the tokens, so few counts are flushed.
 //
 // swiglu_forward: phi = SiLU(gate) * up for every pair row, stored in the input dtype, and
 //   ||phi_u||^2 of the stored row.  Section "LRM: a decomposable contribution score": the score
@@ -27,27 +28,39 @@ template <int MAXM>  // E <= 32 * MAXM
 __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(
     const float* __restrict__ logits, int64_t n_tok, int E, int k, int kind, int32_t num, int32_t den, int32_t cap,
     const int32_t* __restrict__ explicit_q, int32_t* __restrict__ topk_idx, float* __restrict__ alpha,
-    int32_t* __restrict__ loads, int32_t* __restrict__ quotas, uint32_t* __restrict__ done, int32_t* status) {
+    int32_t* __restrict__ loads, int32_t* __restrict__ quotas, uint32_t* __restrict__ done,
+    int32_t* __restrict__ acc, int32_t* status) {
   extern __shared__ int hist[];  // [E]
   __shared__ bool s_last;
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
   const int lane = threadIdx.x & 31;
   const int64_t stride = (int64_t)gridDim.x * kRouteWarps;
-  for (int64_t t = (int64_t)blockIdx.x * kRouteWarps + (threadIdx.x >> 5); t < n_tok; t += stride) {
-    const float* row = logits + t * E;
+  // the next token's logits are loaded while this token's experts are picked
+  float nxt[MAXM];
+  auto load_row = [&](int64_t tt) {
+#pragma unroll
+    for (int m = 0; m < MAXM; ++m) {
+      const int e = lane + 32 * m;
+      nxt[m] = (tt < n_tok && e < E) ? __ldg(logits + tt * E + e) : -INFINITY;
+    }
+  };
+  int64_t t = (int64_t)blockIdx.x * kRouteWarps + (threadIdx.x >> 5);
+  load_row(t);
+  for (; t < n_tok; t += stride) {
     float v[MAXM];
     bool bad = false;
 #pragma unroll
     for (int m = 0; m < MAXM; ++m) {
       const int e = lane + 32 * m;
-      float x = e < E ? row[e] : -INFINITY;
+      float x = nxt[m];
       if (e < E && !isfinite(x)) {
         bad = true;
         x = -INFINITY;  // a non-finite logit is never preferred, and is reported
       }
       v[m] = x;
     }
+    load_row(t + stride);
     if (bad) set_status(status, LRM_ERR_NONFINITE);
     uint32_t taken = 0;  // bit m: expert lane + 32m already chosen
     int my_e = 0;
@@ -90,7 +103,7 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(
   }
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x)
-    if (hist[e]) atomicAdd(&loads[e], hist[e]);
+    if (hist[e]) atomicAdd(&acc[e], hist[e]);
   __threadfence();
   __syncthreads();
   if (threadIdx.x == 0) s_last = atomicAdd(done, 1u) == gridDim.x - 1;
@@ -98,7 +111,8 @@ __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(
   if (!s_last) return;
   __threadfence();
   for (int e = threadIdx.x; e < E; e += blockDim.x) {
-    const int32_t l = *reinterpret_cast<volatile int32_t*>(loads + e);
+    const int32_t l = *reinterpret_cast<volatile int32_t*>(acc + e);
+    loads[e] = l;
     quotas[e] = quota_rule(l, kind, num, den, cap, explicit_q, e);
   }
 }
@@ -155,17 +169,19 @@ __global__ void __launch_bounds__(256) swiglu_fwd_kernel(const T* __restrict__ h
 
 lrm_status launch_route(const float* logits, int64_t T, int32_t E, int32_t k, int kind, int32_t num, int32_t den,
                         int32_t cap, const int32_t* explicit_q, int32_t* topk_idx, float* alpha, int32_t* loads,
-                        int32_t* quotas, uint32_t* done, int32_t* status, cudaStream_t s) {
-  if (cudaMemsetAsync(loads, 0, sizeof(int32_t) * E, s) != cudaSuccess) return LRM_ERR_CUDA;
-  if (cudaMemsetAsync(done, 0, sizeof(uint32_t), s) != cudaSuccess) return LRM_ERR_CUDA;
+                        int32_t* quotas, uint32_t* ws, int32_t* status, cudaStream_t s) {
+  // ws: [0] the finished-CTA counter, [1 .. E] the load accumulators; one memset clears both
+  uint32_t* done = ws;
+  int32_t* acc = reinterpret_cast<int32_t*>(ws + 1);
+  if (cudaMemsetAsync(ws, 0, sizeof(uint32_t) * (E + 1), s) != cudaSuccess) return LRM_ERR_CUDA;
   int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
-  if (blocks > 152 * 8) blocks = 152 * 8;  // grid-stride beyond that: fewer shared-count flushes
+  if (blocks > 152 * 4) blocks = 152 * 4;  // grid-stride beyond that: fewer shared-count flushes
   if (blocks < 1) blocks = 1;              // T = 0 still applies the rule (all loads 0)
   const size_t smem = sizeof(int) * E;
 #define LRM_ROUTE(MAXM)                                                                                   \
   route_kernel<MAXM><<<(unsigned)blocks, 32 * kRouteWarps, smem, s>>>(logits, T, E, k, kind, num, den, cap, \
                                                                       explicit_q, topk_idx, alpha, loads,   \
-                                                                      quotas, done, status)
+                                                                      quotas, done, acc, status)
   if (E <= 128) LRM_ROUTE(4);
   else if (E <= 256) LRM_ROUTE(8);
   else if (E <= 512) LRM_ROUTE(16);

@@ -91,6 +91,65 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ al
   }
 }
 
+// One round trip per token: a lane issues all of its g and phi loads (GV + MAXK * PV 16-byte
+// vectors) before it uses any, so a warp waits for memory once instead of once per row group.
+// Used when that fits in registers (the 8k-token Qwen3 shape: 8 + 8 * 3 vectors per lane).
+template <typename T, int GV, int PV, int MAXK>
+__global__ void __launch_bounds__(128) score_onepass_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
+                                                           const T* __restrict__ phi, int64_t n_tok, int k, int H,
+                                                           int I, float* __restrict__ scores, int32_t* status) {
+  constexpr int VN = VecTraits<T>::N;
+  const int lane = threadIdx.x & 31;
+  const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= n_tok) return;
+  const int nvg = H / VN, nvp = I / VN;
+  const T* gt = g + t * H;
+  const T* pt = phi + t * k * (int64_t)I;
+  const float my_alpha = lane < k ? alpha[t * k + lane] : 0.f;
+  uint4 gb[GV], pb[MAXK][PV];
+#pragma unroll
+  for (int m = 0; m < GV; ++m) {
+    const int v = lane + 32 * m;
+    gb[m] = v < nvg ? ld_stream16(gt + (int64_t)v * VN) : make_uint4(0, 0, 0, 0);
+  }
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j)
+#pragma unroll
+    for (int m = 0; m < PV; ++m) {
+      const int v = lane + 32 * m;
+      pb[j][m] = (j < k && v < nvp) ? ld_stream16(pt + (int64_t)j * I + (int64_t)v * VN) : make_uint4(0, 0, 0, 0);
+    }
+  float gs = 0.f;
+#pragma unroll
+  for (int m = 0; m < GV; ++m) {
+    float f[VN];
+    unpack(gb[m], f);
+#pragma unroll
+    for (int q = 0; q < VN; ++q) gs = fmaf(f[q], f[q], gs);
+  }
+  gs = warp_sum(gs);
+  float mine = 0.f;  // lane j ends up with row j's ||phi||^2
+#pragma unroll
+  for (int j = 0; j < MAXK; ++j) {
+    if (j >= k) break;
+    float ps = 0.f;
+#pragma unroll
+    for (int m = 0; m < PV; ++m) {
+      float f[VN];
+      unpack(pb[j][m], f);
+#pragma unroll
+      for (int q = 0; q < VN; ++q) ps = fmaf(f[q], f[q], ps);
+    }
+    ps = warp_sum(ps);
+    if (lane == j) mine = ps;
+  }
+  if (lane < k) {
+    const float sc = (my_alpha * my_alpha) * gs * mine;
+    scores[t * k + lane] = sc;
+    if (!isfinite(sc)) set_status(status, LRM_ERR_NONFINITE);
+  }
+}
+
 // The same score with ||phi_u||^2 handed in (from a forward that emits it, see forward.cu): one
 // warp per token reads g_t once and writes its k scores; phi itself is not read.
 template <typename T, int GV>
@@ -176,6 +235,12 @@ void launch_score(const float* alpha, const void* g, const void* phi, int64_t T,
   const int64_t blocks = (T + 7) / 8;  // 8 warps (tokens) per CTA
   const int vn = dt == LRM_BF16 ? 8 : 4;
   const int gv = (H / vn + 31) / 32, pv = (I / vn + 31) / 32;  // vectors per lane of a g / phi row
+  if (dt == LRM_BF16 && gv <= 8 && pv <= 3 && k <= 8) {
+    using B = __nv_bfloat16;
+    score_onepass_kernel<B, 8, 3, 8><<<(unsigned)((T + 3) / 4), 128, 0, s>>>(alpha, (const B*)g, (const B*)phi, T, k,
+                                                                          H, I, scores, status);
+    return;
+  }
   const bool fits = gv <= 16 && pv <= 6;
 #define LRM_SCORE_LAUNCH(TYPE, GV, PV)                                                                 \
   score_kernel<TYPE, GV, PV><<<(unsigned)blocks, 256, 0, s>>>(alpha, (const TYPE*)g, (const TYPE*)phi, T, k, H, \
