@@ -7,7 +7,7 @@ resident in HBM.  Default workload: the Qwen3-30B-A3B-shaped layer, T=8192, H=20
 I=768, E=128, top-8, bf16, drop 20 % (quota = ceil(0.8 * load)).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-       [--workload NAME] [--no-cpu-baseline]
+       [--workload NAME] [--no-cpu-baseline] [--no-extras]
 Under torchrun (N > 1) every rank runs an independent batch (weak scaling, no collective on
 the data path; a barrier brackets the timed region and the slowest rank's time is used).
 
@@ -207,6 +207,9 @@ def main():
     ap.add_argument("--workload", default="qwen3_t8k_d20", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05 (comparison only)")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the widened rows timed after the headline step (router gradient, compaction-free, "
+                         "forward-side steps, ablation scores)")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
 
@@ -342,7 +345,7 @@ def main():
     if tr:
         roof["traffic_workload"] = tr["workload"]
 
-    nxt = next_rows(args, wl, inp, quotas, flags, dev, stream, ms_per_step, pk)
+    nxt = None if args.no_extras else next_rows(args, wl, inp, quotas, flags, dev, stream, ms_per_step, pk)
     launches = pb_launches(wl, flags)
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,

@@ -22,7 +22,7 @@ namespace lrm {
 
 namespace {
 
-constexpr int kRouteWarps = 8;
+constexpr int kRouteWarps = 16;  // 512-thread CTAs, two per SM: few count flushes
 
 template <int MAXM>  // E <= 32 * MAXM
 __global__ void __launch_bounds__(32 * kRouteWarps) route_kernel(
@@ -175,7 +175,7 @@ lrm_status launch_route(const float* logits, int64_t T, int32_t E, int32_t k, in
   int32_t* acc = reinterpret_cast<int32_t*>(ws + 1);
   if (cudaMemsetAsync(ws, 0, sizeof(uint32_t) * (E + 1), s) != cudaSuccess) return LRM_ERR_CUDA;
   int64_t blocks = (T + kRouteWarps - 1) / kRouteWarps;
-  if (blocks > 152 * 4) blocks = 152 * 4;  // grid-stride beyond that: fewer shared-count flushes
+  if (blocks > 152 * 2) blocks = 152 * 2;  // grid-stride beyond two CTAs per SM: fewer count flushes
   if (blocks < 1) blocks = 1;              // T = 0 still applies the rule (all loads 0)
   const size_t smem = sizeof(int) * E;
 #define LRM_ROUTE(MAXM)                                                                                   \
