@@ -64,7 +64,8 @@ constexpr int kThreads = 64 + 32 * kEpiWarps + 32 * kGatherExtraWarps;
 // (scalar shared accesses are conflict-free both row-per-thread and row-contiguous).
 constexpr int kVmLd = 33;
 constexpr int kEpiBytes = 32 * kVmLd * 4;
-// var-K: the same region holds one 4 KB, 1024-byte-aligned staging box per warp for TMA stores
+// var-K: the same region holds two 2 KB staging boxes per warp for TMA stores, used in turn
+// (4 KB, 1024-byte-aligned)
 constexpr int kBoxBytes = 4096;
 static_assert(kBoxBytes <= kEpiBytes, "staging box must fit in the per-warp epilogue region");
 constexpr int kTmemCols = 512;
@@ -235,7 +236,7 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
-__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // A tensor map written by another kernel (generic proxy) must be acquired by the tensormap
 // proxy before a TMA instruction uses it.
@@ -650,19 +651,25 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int i = 0; i < 32; ++i) v[i] = 0u;
         if (p.kind == VK) {
-          // fp32 dW: the warp's 32 x 32 block leaves as one TMA tensor store from a
-          // 128-byte-swizzled staging box (the map clips rows >= M and columns >= N)
-          uint8_t* box = reinterpret_cast<uint8_t*>(stg);
-          if (lane == 0) bulk_wait_read_all();  // the previous store has read the box
-          __syncwarp();
-          uint8_t* line = box + lane * 128;
+          // fp32 dW: the warp's 32 x 32 block leaves as two 32-row x 16-column TMA tensor stores
+          // from two 2 KB, 64-byte-swizzled staging boxes used in turn, so that a warp always has
+          // one store in flight while it fills the other box (the map clips rows >= M, columns >= N)
 #pragma unroll
-          for (int jj = 0; jj < 8; ++jj)
-            *reinterpret_cast<uint4*>(line + ((jj ^ (lane & 7)) << 4)) =
-                make_uint4(v[4 * jj], v[4 * jj + 1], v[4 * jj + 2], v[4 * jj + 3]);
-          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-          __syncwarp();
-          if (lane == 0) tma_store_3d(&tmC, smem_u32(box), n, row_base, d.e);
+          for (int hh = 0; hh < 2; ++hh) {
+            uint8_t* box = reinterpret_cast<uint8_t*>(stg) + hh * 2048;
+            if (lane == 0) bulk_wait_read_le1();  // the store before last (this box's) has read it
+            __syncwarp();
+            uint8_t* line = box + lane * 64;
+            const int sw = (lane >> 1) & 3;  // 64-byte swizzle: 16-byte chunk j of row r -> j ^ ((r >> 1) & 3)
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj)
+              *reinterpret_cast<uint4*>(line + ((jj ^ sw) << 4)) =
+                  make_uint4(v[16 * hh + 4 * jj], v[16 * hh + 4 * jj + 1], v[16 * hh + 4 * jj + 2],
+                             v[16 * hh + 4 * jj + 3]);
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncwarp();
+            if (lane == 0) tma_store_3d(&tmC, smem_u32(box), n + 16 * hh, row_base, d.e);
+          }
           continue;
         }
 #pragma unroll
@@ -867,14 +874,14 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K, uint6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// fp32 [E, M, N] output with a {32, 32, 1} box and 128-byte swizzle (the epilogue's staging box).
+// fp32 [E, M, N] output with a {16, 32, 1} box and 64-byte swizzle (the epilogue's 2 KB staging boxes).
 bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t N) {
   const cuuint64_t dims[3] = {N, M, E};
   const cuuint64_t strides[2] = {N * 4, M * N * 4};
-  const cuuint32_t box[3] = {32, 32, 1};
+  const cuuint32_t box[3] = {16, 32, 1};
   const cuuint32_t estr[3] = {1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, estr,
-                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
