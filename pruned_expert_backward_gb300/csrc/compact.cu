@@ -11,9 +11,9 @@
 // scaled by alpha_u) into each kept pair's row; the token's k rows of h and phi are one
 // contiguous span, read only where the pair is kept.  16-byte coalesced loads and stores.
 //
-// scatter_dx: a CTA covers several tokens (up to 512 threads); each thread owns one 16-byte
-// column slice of one token, issues the k row loads together and adds them in j order in
-// fp32 (deterministic, no atomics).
+// scatter_dx: a CTA covers 16 tokens; each thread owns one 16-byte column slice, walks the
+// CTA's kept rows with 8 loads in flight and adds each token's rows in j order in fp32
+// (deterministic, no atomics).
 #include "common.cuh"
 #include "kernels.h"
 
@@ -85,53 +85,73 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   }
 }
 
-template <typename T, int MAXK>
-__global__ void __launch_bounds__(512, MAXK <= 8 ? 2 : 1) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
-                                                          const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
-                                                          int tok_per_blk, T* __restrict__ dx) {
+// A CTA takes kScatterTok consecutive tokens.  Warp 0 lists their kept rows in (token, j) order
+// in shared memory; then every thread walks that list for one 16-byte column slice, keeping
+// kScatterLoads row loads in flight however few rows each token kept, and adds each token's rows
+// in j order in fp32 (deterministic: the same sum in the same order as one row at a time).
+constexpr int kScatterTok = 16;
+constexpr int kScatterLoads = 8;
+
+template <typename T>
+__global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
+                                                         const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
+                                                         T* __restrict__ dx) {
   constexpr int VN = VecTraits<T>::N;
-  extern __shared__ int32_t s_rows[];  // [tok_per_blk][k]
-  const int64_t t0 = (int64_t)blockIdx.x * tok_per_blk;
-  for (int i = threadIdx.x; i < tok_per_blk * k; i += blockDim.x) {
-    const int64_t u = t0 * k + i;
-    s_rows[i] = u < n_tok * k ? row_of_pair[u] : -1;
+  constexpr int B = kScatterLoads;
+  __shared__ int2 s_item[kScatterTok * LRM_MAX_TOPK];  // (token within the CTA, compacted row)
+  __shared__ int s_n;
+  const int64_t t0 = (int64_t)blockIdx.x * kScatterTok;
+  const int ntok = (int)min((int64_t)kScatterTok, n_tok - t0);
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int base = 0;
+    for (int q0 = 0; q0 < ntok * k; q0 += 32) {
+      const int q = q0 + lane;
+      const int r = q < ntok * k ? row_of_pair[t0 * k + q] : -1;
+      const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
+      if (r >= 0) s_item[base + __popc(m & ((1u << lane) - 1u))] = make_int2(q / k, r);
+      base += __popc(m);
+    }
+    if (lane == 0) s_n = base;
   }
   __syncthreads();
+  const int n = s_n;
   const int nvH = H / VN;
-  for (int w = threadIdx.x; w < tok_per_blk * nvH; w += blockDim.x) {
-    const int tt = w / nvH, v = w - tt * nvH;
-    const int64_t t = t0 + tt;
-    if (t >= n_tok) break;
-    const int32_t* srow = s_rows + tt * k;
-    int32_t rows[MAXK];
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) rows[j] = j < k ? srow[j] : -1;
-    uint4 vals[MAXK];
-#pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (rows[j] >= 0) vals[j] = ld_stream16(dx_c + (int64_t)rows[j] * H + v * VN);
-    }
+  for (int v = threadIdx.x; v < nvH; v += blockDim.x) {
     float acc[VN];
 #pragma unroll
     for (int q = 0; q < VN; ++q) acc[q] = 0.f;
+    int cur = 0;  // the token acc belongs to; tokens before it are written
+    for (int b0 = 0; b0 < n; b0 += B) {
+      uint4 vals[B];
 #pragma unroll
-    for (int j = 0; j < MAXK; ++j) {
-      if (rows[j] >= 0) {
+      for (int m = 0; m < B; ++m)
+        if (b0 + m < n) vals[m] = ld_stream16(dx_c + (int64_t)s_item[b0 + m].y * H + (int64_t)v * VN);
+#pragma unroll
+      for (int m = 0; m < B; ++m) {
+        if (b0 + m >= n) break;
+        const int tok = s_item[b0 + m].x;
+        while (cur < tok) {  // cur is complete (tokens with nothing kept get 0)
+          st16(dx + (t0 + cur) * H + (int64_t)v * VN, pack(acc));
+#pragma unroll
+          for (int q = 0; q < VN; ++q) acc[q] = 0.f;
+          ++cur;
+        }
         float f[VN];
-        unpack(vals[j], f);
+        unpack(vals[m], f);
 #pragma unroll
         for (int q = 0; q < VN; ++q) acc[q] += f[q];
       }
     }
-    st16(dx + t * H + v * VN, pack(acc));
+    while (cur < ntok) {
+      st16(dx + (t0 + cur) * H + (int64_t)v * VN, pack(acc));
+#pragma unroll
+      for (int q = 0; q < VN; ++q) acc[q] = 0.f;
+      ++cur;
+    }
   }
 }
 
-int threads_for(int n_vec) {
-  int t = n_vec < 512 ? n_vec : 512;
-  t = (t + 31) / 32 * 32;
-  return t < 32 ? 32 : t;
-}
 
 }  // namespace
 
@@ -155,23 +175,14 @@ void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, 
                        void* dx, cudaStream_t s) {
   if (T == 0) return;
   const int nvH = H / (dt == LRM_BF16 ? 8 : 4);
-  int tok = nvH >= 512 ? 1 : 512 / nvH;  // one thread per 16-byte column slice, up to 512 threads
-  if (tok > 64) tok = 64;
-  const int threads = threads_for(nvH * tok);
-  const unsigned blocks = (unsigned)((T + tok - 1) / tok);
-  const size_t smem = sizeof(int32_t) * tok * k;
-  using B = __nv_bfloat16;
-  if (dt == LRM_BF16 && k <= 8)
-    scatter_dx_kernel<B, 8><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok, (B*)dx);
-  else if (dt == LRM_BF16)
-    scatter_dx_kernel<B, LRM_MAX_TOPK><<<blocks, threads, smem, s>>>(row_of_pair, (const B*)dx_c, T, k, H, tok,
-                                                                     (B*)dx);
-  else if (k <= 8)
-    scatter_dx_kernel<float, 8><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H, tok,
-                                                              (float*)dx);
+  int threads = (nvH + 31) / 32 * 32;  // one thread per 16-byte column slice (warp 0 also builds the list)
+  if (threads > 256) threads = 256;
+  const unsigned blocks = (unsigned)((T + kScatterTok - 1) / kScatterTok);
+  if (dt == LRM_BF16)
+    scatter_dx_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(row_of_pair, (const __nv_bfloat16*)dx_c, T, k, H,
+                                                                (__nv_bfloat16*)dx);
   else
-    scatter_dx_kernel<float, LRM_MAX_TOPK><<<blocks, threads, smem, s>>>(row_of_pair, (const float*)dx_c, T, k, H,
-                                                                         tok, (float*)dx);
+    scatter_dx_kernel<float><<<blocks, threads, 0, s>>>(row_of_pair, (const float*)dx_c, T, k, H, (float*)dx);
 }
 
 }  // namespace lrm
