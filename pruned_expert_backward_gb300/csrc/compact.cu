@@ -31,20 +31,25 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   constexpr int VN = VecTraits<T>::N;
   __shared__ int64_t s_row[LRM_MAX_TOPK];
   __shared__ float s_alpha[LRM_MAX_TOPK];
-  __shared__ int s_any;
+  __shared__ int s_kept[LRM_MAX_TOPK];  // the token's kept choices j, ascending
+  __shared__ int s_nk;
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, nt = blockDim.x;
-  if (tid == 0) s_any = 0;
-  __syncthreads();
-  if (tid < k) {
-    const int r = row_of_pair[t * k + tid];
-    const bool kept = r >= 0 && (int64_t)r < cap;
-    s_row[tid] = kept ? (int64_t)r : -1;
-    s_alpha[tid] = alpha[t * k + tid];
-    if (kept) s_any = 1;
+  if (tid < 32) {
+    int r = -1;
+    if (tid < k) {
+      r = row_of_pair[t * k + tid];
+      if ((int64_t)r >= cap) r = -1;
+      s_row[tid] = r;
+      s_alpha[tid] = alpha[t * k + tid];
+    }
+    const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
+    if (r >= 0) s_kept[__popc(m & ((1u << tid) - 1u))] = tid;
+    if (tid == 0) s_nk = __popc(m);
   }
   __syncthreads();
-  if (!s_any) return;
+  const int nk = s_nk;
+  if (nk == 0) return;
 
   const int nvH = H / VN;
   const T* gt = g + t * H;
@@ -54,9 +59,9 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
     const uint4 xv = x_c != nullptr ? ld_stream16(xt + v * VN) : make_uint4(0, 0, 0, 0);
     float f[VN];
     unpack(gv, f);
-    for (int j = 0; j < k; ++j) {
+    for (int jj = 0; jj < nk; ++jj) {
+      const int j = s_kept[jj];
       const int64_t r = s_row[j];
-      if (r < 0) continue;
       const float a = s_alpha[j];
       float o[VN];
 #pragma unroll
@@ -67,21 +72,20 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   }
   if (h_c == nullptr) return;  // compaction-free variant: only the scaled gradient rows
 
+  // the kept pairs' h and phi rows only (v runs over kept rows x vectors)
   const int nv2 = 2 * I / VN;
   const T* ht = h + t * k * (int64_t)(2 * I);
-  for (int v = tid; v < k * nv2; v += nt) {
-    const int j = v / nv2;
-    const int64_t r = s_row[j];
-    if (r < 0) continue;
-    st16(h_c + r * (2 * I) + (v - j * nv2) * VN, ld_stream16(ht + (int64_t)v * VN));
+  for (int v = tid; v < nk * nv2; v += nt) {
+    const int jj = v / nv2, c = v - jj * nv2;
+    const int j = s_kept[jj];
+    st16(h_c + s_row[j] * (2 * I) + c * VN, ld_stream16(ht + ((int64_t)j * nv2 + c) * VN));
   }
   const int nv1 = I / VN;
   const T* pt = phi + t * k * (int64_t)I;
-  for (int v = tid; v < k * nv1; v += nt) {
-    const int j = v / nv1;
-    const int64_t r = s_row[j];
-    if (r < 0) continue;
-    st16(phi_c + r * I + (v - j * nv1) * VN, ld_stream16(pt + (int64_t)v * VN));
+  for (int v = tid; v < nk * nv1; v += nt) {
+    const int jj = v / nv1, c = v - jj * nv1;
+    const int j = s_kept[jj];
+    st16(phi_c + s_row[j] * I + c * VN, ld_stream16(pt + ((int64_t)j * nv1 + c) * VN));
   }
 }
 
