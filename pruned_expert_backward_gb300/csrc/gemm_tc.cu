@@ -632,13 +632,28 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
       const Tile d = decode(p, t, rank);
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
+      const int row_base = p.kind == VK ? d.m0 + q * 32 : d.row0 + q * 32;
+      const int row_lim = p.kind == VK ? p.M : d.row_end;
+      const int nrows = d.has_rows ? min(32, row_lim - row_base) : 0;
+      if (p.kind == VM_SWIGLU && lane < nrows) {
+        // while the tile's MMAs run, pull this warp's gate and up rows (its 128 columns of
+        // each) into L2, so that the SwiGLU epilogue below reads them from L2
+        const int I = p.N, col = d.n0 + half * 128;
+        const __nv_bfloat16* hrow = p.kept_pair ? p.gsrc + (int64_t)__ldg(p.kept_pair + row_base + lane) * 2 * I
+                                                : p.h_c + (int64_t)(row_base + lane) * 2 * I;
+        if (col < I) {
+#pragma unroll
+          for (int b = 0; b < 2; ++b) {
+            if (col + b * 64 >= I) break;
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(hrow + col + b * 64));
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(hrow + I + col + b * 64));
+          }
+        }
+      }
       if (!mbar_wait(accf0 + 8 * acc, acc_ph, abortv, p.status)) break;
       tc_fence_after();
       const uint32_t tbase = tmem_base + acc * kBN + ((uint32_t)(q * 32) << 16);
       const bool have_acc = d.k_iters > 0;
-      const int row_base = p.kind == VK ? d.m0 + q * 32 : d.row0 + q * 32;
-      const int row_lim = p.kind == VK ? p.M : d.row_end;
-      const int nrows = d.has_rows ? min(32, row_lim - row_base) : 0;
       // VM_SWIGLU: this lane's part of dphi . phi for rows i*8 + sub over its columns, where
       // dphi . phi = sum of dup * up (dup = dphi * gate * s, phi = gate * s * up)
       float rdot[4] = {0.f, 0.f, 0.f, 0.f};
