@@ -99,6 +99,13 @@ struct TcParams {
   const __nv_bfloat16* gsrc;
   int gk;   // VK: > 0 when the gathered rows are tokens (u / gk)
   int gld;  // elements per row of gsrc
+  // MN-major operands whose 64-column blocks come in one TMA box: the map views the operand as
+  // [column block][K line][64 columns], so one {64, 64, 2} box fills both 8 KB blocks of a CTA's
+  // 128 columns (the same shared-memory layout as two {64, 64} boxes, in one instruction).
+  // Only where the column count is a multiple of 64 (a partial block would wrap into the next
+  // line instead of being zero-filled).
+  int merged_a;  // VK: A
+  int merged_b;  // VK and VM: B
 };
 
 // ---------------------------------------------------------------- PTX wrappers -------
@@ -207,6 +214,14 @@ __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap
       "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
       "%3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
+      : "memory");
+}
+__device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
+                                                 uint32_t cbar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
+      "%3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(cbar)
       : "memory");
 }
 // 16-byte cp.async into shared memory; src_bytes < 16 zero-fills the rest (0: nothing is read).
@@ -457,8 +472,12 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (gw == 0 && lane == 0) {
         mbar_expect_tx_cluster(fb, d.has_rows ? kABytes : 0);
         if (d.has_rows) {
-          tma_load_2d_pair(a_dst, ma, d.m0, r0, fb);
-          tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r0, fb);
+          if (p.merged_a) {
+            tma_load_3d_pair(a_dst, ma, 0, r0, d.m0 / 64, fb);
+          } else {
+            tma_load_2d_pair(a_dst, ma, d.m0, r0, fb);
+            tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r0, fb);
+          }
         }
       }
       // source rows (pairs, or their tokens) of K rows lane and lane + 32
@@ -524,15 +543,27 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (p.kind == VK) {
             const int r = d.row0 + kb * kBK;
             if (d.has_rows) {
-              tma_load_2d_pair(a_dst, ma, d.m0, r, fb);
-              tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r, fb);
+              if (p.merged_a) {
+                tma_load_3d_pair(a_dst, ma, 0, r, d.m0 / 64, fb);
+              } else {
+                tma_load_2d_pair(a_dst, ma, d.m0, r, fb);
+                tma_load_2d_pair(a_dst + 8192, ma, d.m0 + 64, r, fb);
+              }
             }
-            tma_load_2d_pair(b_dst, mb, nb, r, fb);
-            tma_load_2d_pair(b_dst + 8192, mb, nb + 64, r, fb);
+            if (p.merged_b) {
+              tma_load_3d_pair(b_dst, mb, 0, r, nb / 64, fb);
+            } else {
+              tma_load_2d_pair(b_dst, mb, nb, r, fb);
+              tma_load_2d_pair(b_dst + 8192, mb, nb + 64, r, fb);
+            }
           } else {
             if (d.has_rows) tma_load_2d_pair(a_dst, &tmA, kb * kBK, d.row0, fb);
-            tma_load_3d_pair(b_dst, &tmB, nb, kb * kBK, d.e, fb);
-            tma_load_3d_pair(b_dst + 8192, &tmB, nb + 64, kb * kBK, d.e, fb);
+            if (p.merged_b) {
+              tma_load_4d_pair(b_dst, &tmB, 0, kb * kBK, nb / 64, d.e, fb);
+            } else {
+              tma_load_3d_pair(b_dst, &tmB, nb, kb * kBK, d.e, fb);
+              tma_load_3d_pair(b_dst + 8192, &tmB, nb + 64, kb * kBK, d.e, fb);
+            }
           }
         }
       }
@@ -889,6 +920,30 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K, uint6
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// bf16 row-major [rows, cols] viewed as [cols / 64 blocks][rows][64] with a {64, 64, 2} box: one box
+// fills a CTA's two 64-column blocks of a 64-line K slice (cols a multiple of 64).
+bool make_map_blocks_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[3] = {64, rows, cols / 64};
+  const cuuint64_t strides[2] = {cols * 2, 128};
+  const cuuint32_t box[3] = {64, 64, 2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// bf16 [E, K, N] viewed as [E][N / 64 blocks][K][64] with a {64, 64, 2, 1} box (N a multiple of 64).
+bool make_map_blocks_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K, uint64_t N) {
+  const cuuint64_t dims[4] = {64, K, N / 64, E};
+  const cuuint64_t strides[3] = {N * 2, 128, K * N * 2};
+  const cuuint32_t box[4] = {64, 64, 2, 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// Column counts whose 64-column blocks may share one box (see TcParams::merged_a).
+bool mergeable(uint64_t cols) { return cols % 64 == 0 && cols >= 128; }
+
 // fp32 [E, M, N] output with a {16, 32, 1} box and 64-byte swizzle (the epilogue's 2 KB staging boxes).
 bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t N) {
   const cuuint64_t dims[3] = {N, M, E};
@@ -973,11 +1028,21 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   MapTemplates tpl;
   const bool gather = g.kept_pair != nullptr;  // compaction-free: phi / x rows gathered by index
   // (gathering, the B templates are never used; they are encoded over dy_c only to stay valid)
-  if (!make_map_2d(&tpl.t[0], g.dy_c, rows, H, 64) ||
-      !make_map_2d(&tpl.t[1], gather ? g.dy_c : g.phi_c, rows, I, 64) ||
-      !make_map_2d(&tpl.t[2], g.dh_c, rows, 2 * I, 64) ||
-      !make_map_2d(&tpl.t[3], gather ? g.dy_c : g.x_c, rows, H, 64))
+  // var-K operand maps (MN-major): one box per CTA and K slice where the column count allows (the
+  // two-box form otherwise, or if the driver declines the blocked view)
+  bool merged[4];
+  auto vk_map = [&](int j, const void* base, uint64_t cols) {
+    merged[j] = mergeable(cols) && make_map_blocks_2d(&tpl.t[j], base, rows, cols);
+    return merged[j] || make_map_2d(&tpl.t[j], base, rows, cols, 64);
+  };
+  if (!vk_map(0, g.dy_c, H) || !vk_map(1, gather ? g.dy_c : g.phi_c, I) || !vk_map(2, g.dh_c, 2 * I) ||
+      !vk_map(3, gather ? g.dy_c : g.x_c, H))
     return LRM_ERR_CUDA;
+  // var-M weight maps: [E, K, N], blocked the same way where N allows
+  auto vm_map = [&](CUtensorMap* m, const void* base, uint64_t K, uint64_t N, int* merged_b) {
+    *merged_b = mergeable(N) && make_map_blocks_3d(m, base, E, K, N);
+    return *merged_b || make_map_3d(m, base, E, K, N);
+  };
   tc_plan_kernel<<<1, 1024, 0, s>>>(g.seg_offsets, E, plan, maps, tpl);
   if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
 
@@ -985,17 +1050,18 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   const int64_t vm_bound = ((int64_t)g.cap + 2 * kBM - 1) / (2 * kBM) + E;  // pair tiles along M
   lrm_status st;
   // dphi = dy_c W_down[e], SwiGLU backward fused -> dh_c
-  if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !make_map_3d(&mB, g.w_down, E, H, I)) return LRM_ERR_CUDA;
+  int vm_merged = 0;
+  if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !vm_map(&mB, g.w_down, H, I, &vm_merged)) return LRM_ERR_CUDA;
   using B16 = const __nv_bfloat16*;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
              (B16)g.h_c, g.status, nullptr, nullptr, g.dot_part, (I + 127) / 128,
-             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I};
+             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I, 0, vm_merged};
   if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   if (g.row_dot != nullptr) launch_row_dot(g.dot_part, p.n_part, g.seg_offsets, E, g.cap, g.row_dot, s);
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
                nullptr, g.status, maps + 0 * E, maps + 1 * E, nullptr, 0,
-               g.kept_pair, gather ? (B16)g.phi : nullptr, 0, I};
+               g.kept_pair, gather ? (B16)g.phi : nullptr, 0, I, merged[0], merged[1]};
   mA = tpl.t[0];
   mB = tpl.t[1];
   CUtensorMap mC;
@@ -1004,16 +1070,17 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
   p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
                g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E, nullptr, 0,
-               g.kept_pair, gather ? (B16)g.x : nullptr, g.k, H};
+               g.kept_pair, gather ? (B16)g.x : nullptr, g.k, H, merged[2], merged[3]};
   mA = tpl.t[2];
   mB = tpl.t[3];
   if (!make_map_out3d(&mC, g.dw_gate_up, E, 2 * I, H)) return LRM_ERR_CUDA;
   if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dx_c = dh_c W_gate_up[e]  (K = 2I, N = H)
-  if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !make_map_3d(&mB, g.w_gate_up, E, 2 * I, H))
+  if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !vm_map(&mB, g.w_gate_up, 2 * I, H, &vm_merged))
     return LRM_ERR_CUDA;
   p = TcParams{VM_STORE, E, 0, H, 2 * I, 0, (H + kBN - 1) / kBN, g.seg_offsets, plan, g.dx_c, nullptr,
                g.status, nullptr, nullptr};
+  p.merged_b = vm_merged;
   if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   return LRM_OK;
 }
