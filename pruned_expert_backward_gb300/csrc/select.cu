@@ -13,10 +13,12 @@
 //              then scatters its pairs stably into the expert buckets (u ascending) with
 //              their score bits: ranks within a warp from __match_any_sync, across warps from
 //              per-warp expert counts.
-//  4. expert:  one CTA per expert: MSD radix select (4 x 8 bits) of the quota-th largest
-//              score in the bucket, then one ordered pass that keeps everything above the
-//              threshold plus the first `need` pairs equal to it, and writes kept_pair and
-//              row_of_pair through a block-wide prefix sum.
+//  4. expert:  one CTA per expert (1024 threads, the bucket's keys held in shared memory
+//              when they fit): MSD radix select (up to 4 x 8 bits, stopping early once the
+//              bin of the quota-th largest score is kept whole) of that score, then one
+//              ordered pass that keeps everything above the threshold plus the first `need`
+//              pairs equal to it, and writes kept_pair and row_of_pair through a block-wide
+//              prefix sum.
 // Scores are finite and >= 0, so their IEEE bit patterns order like their values.
 #include "common.cuh"
 #include "kernels.h"
@@ -182,17 +184,21 @@ __global__ void __launch_bounds__(kSelChunk) sel_bucket_kernel(
   }
 }
 
-constexpr int kExpThreads = 512;
+constexpr int kExpThreads = 1024;
 constexpr int kExpIPT = 8;  // bucket elements per thread per round
+// A bucket of up to this many keys is copied into shared memory once and every pass reads it
+// there (192 KB); a larger one is read from global memory on every pass.
+constexpr int kExpSmemKeys = 49152;
 
 __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
     const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u,
     const uint32_t* __restrict__ sorted_key, int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair) {
+  extern __shared__ uint32_t s_keys[];  // [kExpSmemKeys]
   __shared__ int sm[33];
   __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need;
+  __shared__ int s_need, s_whole;
   const int e = blockIdx.x, tid = threadIdx.x;
   const int b0 = bucket_start[e];
   const int load = bucket_start[e + 1] - b0;
@@ -214,9 +220,32 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     return;
   }
 
-  // MSD radix select: find the key value `thr` of the keep-th largest key, and how many of
-  // the keys equal to thr are kept (`need`, >= 1).
-  uint32_t prefix = 0;
+  // the keys every pass reads: a shared-memory copy when the bucket fits
+  const uint32_t* ks = bk;
+  if (load <= kExpSmemKeys) {
+    for (int i0 = 0; i0 < load; i0 += kExpThreads * 8) {
+      uint32_t v[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {  // all eight loads in flight before any store
+        const int i = i0 + q * kExpThreads + tid;
+        v[q] = i < load ? bk[i] : 0u;
+      }
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int i = i0 + q * kExpThreads + tid;
+        if (i < load) s_keys[i] = v[q];
+      }
+    }
+    ks = s_keys;
+    __syncthreads();
+  }
+
+  // MSD radix select, 8 bits a pass: find the key value `thr` of the keep-th largest key and
+  // how many of the keys equal to it are kept (`need`).  When the bin that holds the keep-th
+  // largest key is kept whole, no finer pass is needed: every key >= the bin's lowest value
+  // is kept, which is the rule key > thr with thr = that value - 1 and need = 0 (the value is
+  // > 0 there, because keep < load).
+  uint32_t prefix = 0, thr = 0;
   int need = keep;
 #pragma unroll 1
   for (int pass = 0; pass < 4; ++pass) {
@@ -227,9 +256,9 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     for (int i0 = 0; i0 < load; i0 += kExpThreads * 8) {  // warp-uniform trip count
       uint32_t keys[8];
 #pragma unroll
-      for (int q = 0; q < 8; ++q) {  // all eight loads in flight before any is used
+      for (int q = 0; q < 8; ++q) {
         const int i = i0 + q * kExpThreads + tid;
-        keys[q] = i < load ? bk[i] : 0u;
+        keys[q] = i < load ? ks[i] : 0u;
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
@@ -250,13 +279,20 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     if (tid < 256 && above < need && above + cnt >= need) {
       s_prefix = prefix | ((uint32_t)bin << shift);
       s_need = need - above;
+      s_whole = above + cnt == need;
     }
     __syncthreads();
     prefix = s_prefix;
     need = s_need;
+    const bool whole = s_whole;
     __syncthreads();
+    if (whole) {
+      thr = prefix - 1u;
+      need = 0;
+      break;
+    }
+    thr = prefix;
   }
-  const uint32_t thr = prefix;
 
   // Ordered keep pass.
   int run_eq = 0, run_kept = 0;
@@ -267,7 +303,7 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
 #pragma unroll
     for (int q = 0; q < kExpIPT; ++q) {
       const int i = i0 + q;
-      keys[q] = i < load ? bk[i] : 0u;
+      keys[q] = i < load ? ks[i] : 0u;
       n_eq += (i < load && keys[q] == thr);
     }
     int tot_eq;
@@ -317,9 +353,16 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
   sel_bucket_kernel<<<nc > 0 ? (unsigned)nc : 1u, kSelChunk, bsmem, s>>>(
       topk_idx, scores, P, E, nc, ws.counts, ws.loads, quotas, cap, ws.bucket_start, ws.keep, seg_offsets,
       ws.sorted_u, ws.sorted_key, row_of_pair, status);
-  if (P > 0)
-    sel_expert_kernel<<<E, kExpThreads, 0, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u, ws.sorted_key,
-                                               kept_pair, row_of_pair);
+  if (P > 0) {
+    static bool attr_set = false;
+    const int smem = kExpSmemKeys * (int)sizeof(uint32_t);
+    if (!attr_set) {
+      cudaFuncSetAttribute(sel_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+      attr_set = true;
+    }
+    sel_expert_kernel<<<E, kExpThreads, smem, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u,
+                                                  ws.sorted_key, kept_pair, row_of_pair);
+  }
 }
 
 }  // namespace lrm
