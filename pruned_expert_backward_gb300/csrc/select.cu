@@ -14,11 +14,11 @@
 //              their score bits: ranks within a warp from __match_any_sync, across warps from
 //              per-warp expert counts.
 //  4. expert:  one CTA per expert (1024 threads, the bucket's keys held in shared memory
-//              when they fit): MSD radix select (up to 4 x 8 bits, stopping early once the
-//              bin of the quota-th largest score is kept whole) of that score, then one
-//              ordered pass that keeps everything above the threshold plus the first `need`
-//              pairs equal to it, and writes kept_pair and row_of_pair through a block-wide
-//              prefix sum.
+//              when they fit): MSD radix select of the quota-th largest score over 11 + 11 +
+//              10 bits, each pass after the first reading only the keys left in the chosen
+//              bin (stopping early once that bin is kept whole), then one ordered pass that
+//              keeps everything above the threshold plus the first `need` pairs equal to it,
+//              and writes kept_pair and row_of_pair through ballots and a prefix over warps.
 // Scores are finite and >= 0, so their IEEE bit patterns order like their values.
 #include "common.cuh"
 #include "kernels.h"
@@ -185,21 +185,52 @@ __global__ void __launch_bounds__(kSelChunk) sel_bucket_kernel(
 }
 
 constexpr int kExpThreads = 1024;
-constexpr int kExpIPT = 8;  // bucket elements per thread per round
-// A bucket of up to this many keys is copied into shared memory once and every pass reads it
-// there (192 KB); a larger one is read from global memory on every pass.
-constexpr int kExpSmemKeys = 49152;
+constexpr int kExpWarps = kExpThreads / 32;
+constexpr int kExpBins = 2048;  // radix digits of 11, 11 and 10 bits
+// Shared memory of the per-expert kernel: the digit histogram, the bucket's keys when they fit
+// (read once from global memory instead of on every pass) and the candidate keys left after a
+// pass (those in the bin of the quota-th largest key), which the next pass reads instead of
+// the whole bucket.
+constexpr int kExpKeysCap = 36864;  // 144 KB
+constexpr int kExpCandCap = 18432;  // 72 KB
+constexpr size_t kExpSmemBytes = sizeof(int) * kExpBins + sizeof(uint32_t) * (kExpKeysCap + kExpCandCap);
+
+// Exclusive prefix over the block's warps of one int per warp (lane 0's value counts); every
+// thread gets its warp's prefix and the block total.  `sm` needs 33 ints.
+__device__ __forceinline__ int warp_excl_scan(int v, int* total, int* sm) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (lane == 0) sm[warp] = v;
+  __syncthreads();
+  if (warp == 0) {
+    const int w = lane < kExpWarps ? sm[lane] : 0;
+    int incl = w;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += y;
+    }
+    sm[lane] = incl - w;
+    if (lane == 31) sm[32] = incl;
+  }
+  __syncthreads();
+  const int res = sm[warp];
+  *total = sm[32];
+  __syncthreads();
+  return res;
+}
 
 __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
     const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u,
     const uint32_t* __restrict__ sorted_key, int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair) {
-  extern __shared__ uint32_t s_keys[];  // [kExpSmemKeys]
+  extern __shared__ uint32_t s_dyn[];
+  int* hist = reinterpret_cast<int*>(s_dyn);  // [kExpBins]
+  uint32_t* s_keys = s_dyn + kExpBins;        // [kExpKeysCap]
+  uint32_t* s_cand = s_keys + kExpKeysCap;    // [kExpCandCap]
   __shared__ int sm[33];
-  __shared__ int hist[256];
   __shared__ uint32_t s_prefix;
-  __shared__ int s_need, s_whole;
-  const int e = blockIdx.x, tid = threadIdx.x;
+  __shared__ int s_need, s_whole, s_cnt, s_fill;
+  const int e = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int b0 = bucket_start[e];
   const int load = bucket_start[e + 1] - b0;
   const int keep = keep_arr[e];
@@ -220,9 +251,9 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     return;
   }
 
-  // the keys every pass reads: a shared-memory copy when the bucket fits
+  // the bucket's keys: a shared-memory copy when they fit
   const uint32_t* ks = bk;
-  if (load <= kExpSmemKeys) {
+  if (load <= kExpKeysCap) {
     for (int i0 = 0; i0 < load; i0 += kExpThreads * 8) {
       uint32_t v[8];
 #pragma unroll
@@ -237,103 +268,157 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
       }
     }
     ks = s_keys;
-    __syncthreads();
   }
 
-  // MSD radix select, 8 bits a pass: find the key value `thr` of the keep-th largest key and
-  // how many of the keys equal to it are kept (`need`).  When the bin that holds the keep-th
-  // largest key is kept whole, no finer pass is needed: every key >= the bin's lowest value
-  // is kept, which is the rule key > thr with thr = that value - 1 and need = 0 (the value is
-  // > 0 there, because keep < load).
+  // MSD radix select over 11 + 11 + 10 bits: find the value `thr` of the keep-th largest key and
+  // how many of the keys equal to it are kept (`need`).  A pass looks only at the keys whose
+  // higher digits equal `prefix`: after the first pass those are copied into s_cand (when they
+  // fit), so that later passes read only them.  When the bin holding the keep-th largest key is
+  // kept whole, no finer pass is needed: every key >= the bin's lowest value is kept, which is
+  // the rule key > thr with thr = that value - 1 and need = 0 (the value is > 0 there, because
+  // keep < load).
   uint32_t prefix = 0, thr = 0;
   int need = keep;
+  const uint32_t* src = ks;  // what the current pass reads
+  int n_src = load;
+  bool src_filtered = false;  // src holds only keys that match prefix
 #pragma unroll 1
-  for (int pass = 0; pass < 4; ++pass) {
-    const int shift = 24 - 8 * pass;
-    const uint32_t hi_mask = pass == 0 ? 0u : (0xffffffffu << (32 - 8 * pass));
-    if (tid < 256) hist[tid] = 0;
+  for (int pass = 0; pass < 3; ++pass) {
+    const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+    const uint32_t digit_mask = pass == 2 ? 1023u : 2047u;
+    const uint32_t hi_mask = pass == 0 ? 0u : (pass == 1 ? 0xffe00000u : 0xfffffc00u);
+    for (int b = tid; b < kExpBins; b += kExpThreads) hist[b] = 0;
     __syncthreads();
-    for (int i0 = 0; i0 < load; i0 += kExpThreads * 8) {  // warp-uniform trip count
+    for (int i0 = 0; i0 < n_src; i0 += kExpThreads * 8) {  // warp-uniform trip count
       uint32_t keys[8];
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int i = i0 + q * kExpThreads + tid;
-        keys[q] = i < load ? ks[i] : 0u;
+        keys[q] = i < n_src ? src[i] : 0u;
       }
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int i = i0 + q * kExpThreads + tid;
-        const bool in = i < load && (keys[q] & hi_mask) == prefix;
-        const int bin = in ? (int)((keys[q] >> shift) & 255u) : -1;
+        const bool in = i < n_src && (src_filtered || (keys[q] & hi_mask) == prefix);
+        const int bin = in ? (int)((keys[q] >> shift) & digit_mask) : -1;
         // scores cluster in a few bins: aggregate per warp before touching shared memory
         const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (in && (tid & 31) == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
       }
     }
     __syncthreads();
-    // suffix counts over bins, highest bin first: thread b' handles bin 255 - b'
-    const int bin = 255 - tid;
-    const int cnt = tid < 256 ? hist[bin] : 0;
+    // suffix counts over bins, highest first: thread i takes bins 2047 - 2i and 2046 - 2i
+    const int bhi = kExpBins - 1 - 2 * tid, blo = bhi - 1;
+    const int chi = hist[bhi], clo = hist[blo];
     int tot;
-    const int above = block_excl_scan(cnt, &tot, sm);  // keys in bins > bin
-    if (tid < 256 && above < need && above + cnt >= need) {
-      s_prefix = prefix | ((uint32_t)bin << shift);
+    const int above = block_excl_scan(chi + clo, &tot, sm);  // keys in bins > bhi
+    if (above < need && above + chi >= need) {
+      s_prefix = prefix | ((uint32_t)bhi << shift);
       s_need = need - above;
-      s_whole = above + cnt == need;
+      s_whole = above + chi == need;
+      s_cnt = chi;
+    } else if (above + chi < need && above + chi + clo >= need) {
+      s_prefix = prefix | ((uint32_t)blo << shift);
+      s_need = need - above - chi;
+      s_whole = above + chi + clo == need;
+      s_cnt = clo;
     }
+    if (tid == 0) s_fill = 0;
     __syncthreads();
     prefix = s_prefix;
     need = s_need;
     const bool whole = s_whole;
-    __syncthreads();
+    const int cnt = s_cnt;
     if (whole) {
       thr = prefix - 1u;
       need = 0;
       break;
     }
     thr = prefix;
+    if (pass == 2) break;
+    // keep only the keys of the chosen bin for the next pass (in place when src is s_cand: a
+    // batch is read into registers before any of it is overwritten, and the write position never
+    // passes the read position)
+    if (cnt <= kExpCandCap) {
+      const uint32_t sel_mask = pass == 0 ? 0xffe00000u : 0xfffffc00u;
+      for (int i0 = 0; i0 < n_src; i0 += kExpThreads * 8) {
+        uint32_t keys[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = i0 + q * kExpThreads + tid;
+          keys[q] = i < n_src ? src[i] : 0u;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int i = i0 + q * kExpThreads + tid;
+          const bool m = i < n_src && (keys[q] & sel_mask) == prefix;
+          const unsigned bal = __ballot_sync(0xffffffffu, m);
+          int off = 0;
+          if (lane == 0 && bal) off = atomicAdd(&s_fill, __popc(bal));
+          off = __shfl_sync(0xffffffffu, off, 0);
+          if (m) s_cand[off + __popc(bal & ((1u << lane) - 1u))] = keys[q];
+        }
+        __syncthreads();
+      }
+      src = s_cand;
+      n_src = cnt;
+      src_filtered = true;
+    } else {
+      src_filtered = false;  // too many to copy: the next pass reads all keys and matches prefix
+      src = ks;
+      n_src = load;
+    }
+    __syncthreads();
   }
 
-  // Ordered keep pass.
+  // Ordered keep pass.  A round covers kExpThreads * 8 keys; warp w takes 256 consecutive keys,
+  // lane l the keys w * 256 + q * 32 + l (q = 0..7), so reads are coalesced and conflict-free and
+  // the bucket order is kept through ballots.
+  const unsigned lt_mask = (1u << lane) - 1u;
   int run_eq = 0, run_kept = 0;
-  for (int r0 = 0; r0 < load; r0 += kExpThreads * kExpIPT) {
-    const int i0 = r0 + tid * kExpIPT;
-    uint32_t keys[kExpIPT];
-    int n_eq = 0;
+  for (int r0 = 0; r0 < load; r0 += kExpThreads * 8) {
+    const int wb = r0 + warp * 256;
+    uint32_t keys[8];
+    unsigned eqm[8];
+    int w_eq = 0;
 #pragma unroll
-    for (int q = 0; q < kExpIPT; ++q) {
-      const int i = i0 + q;
+    for (int q = 0; q < 8; ++q) {
+      const int i = wb + q * 32 + lane;
       keys[q] = i < load ? ks[i] : 0u;
-      n_eq += (i < load && keys[q] == thr);
+      eqm[q] = __ballot_sync(0xffffffffu, i < load && keys[q] == thr);
+      w_eq += __popc(eqm[q]);
     }
     int tot_eq;
-    int eq_rank = run_eq + block_excl_scan(n_eq, &tot_eq, sm);
-    bool kf[kExpIPT];
-    int n_kept = 0;
+    int eq_before = run_eq + warp_excl_scan(w_eq, &tot_eq, sm);
+    unsigned kfm[8];
+    int w_kept = 0;
 #pragma unroll
-    for (int q = 0; q < kExpIPT; ++q) {
-      const int i = i0 + q;
-      const bool in = i < load;
-      const bool is_eq = in && keys[q] == thr;
-      kf[q] = in && (keys[q] > thr || (is_eq && eq_rank < need));
-      eq_rank += is_eq;
-      n_kept += kf[q];
+    for (int q = 0; q < 8; ++q) {
+      const int i = wb + q * 32 + lane;
+      const bool is_eq = (eqm[q] >> lane) & 1u;
+      const int eq_rank = eq_before + __popc(eqm[q] & lt_mask);
+      const bool kf = i < load && (keys[q] > thr || (is_eq && eq_rank < need));
+      eq_before += __popc(eqm[q]);
+      kfm[q] = __ballot_sync(0xffffffffu, kf);
+      w_kept += __popc(kfm[q]);
     }
     int tot_kept;
-    int pos = run_kept + block_excl_scan(n_kept, &tot_kept, sm);
+    int pos = run_kept + warp_excl_scan(w_kept, &tot_kept, sm);
 #pragma unroll
-    for (int q = 0; q < kExpIPT; ++q) {
-      const int i = i0 + q;
+    for (int q = 0; q < 8; ++q) {
+      const int i = wb + q * 32 + lane;
       if (i < load) {
         const int u = bu[i];
-        if (kf[q]) {
-          kept_pair[base + pos] = u;
-          row_of_pair[u] = base + pos;
-          ++pos;
+        if ((kfm[q] >> lane) & 1u) {
+          const int r = base + pos + __popc(kfm[q] & lt_mask);
+          kept_pair[r] = u;
+          row_of_pair[u] = r;
         } else {
           row_of_pair[u] = -1;
         }
       }
+      pos += __popc(kfm[q]);
     }
     run_eq += tot_eq;
     run_kept += tot_kept;
@@ -355,7 +440,7 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
       ws.sorted_u, ws.sorted_key, row_of_pair, status);
   if (P > 0) {
     static bool attr_set = false;
-    const int smem = kExpSmemKeys * (int)sizeof(uint32_t);
+    const int smem = (int)kExpSmemBytes;
     if (!attr_set) {
       cudaFuncSetAttribute(sel_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       attr_set = true;
