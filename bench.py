@@ -475,7 +475,7 @@ def next_rows(args, wl, inp, quotas, flags, dev, stream, ms_step, pk):
 
 def pb_launches(wl, flags):
     """Kernels this library launches per step (memsets excluded)."""
-    sel = 4 if wl.P > 0 else 1
+    sel = (5 if wl.P >= 131072 else 4) if wl.P > 0 else 1  # the row scatter runs from 131072 pairs on
     grouped = 4 if flags else 5  # SIMT: 4 GEMMs; tcgen05: tile-plan kernel + 4 GEMMs
     return 1 + sel + 1 + grouped + 1
 

@@ -19,6 +19,8 @@
 //              bin (stopping early once that bin is kept whole), then one ordered pass that
 //              keeps everything above the threshold plus the first `need` pairs equal to it,
 //              and writes kept_pair and row_of_pair through ballots and a prefix over warps.
+//  5. rows:    (from 131072 pairs on) scatters row_of_pair from the rows step 4 left in bucket
+//              order, on the whole GPU.
 // Scores are finite and >= 0, so their IEEE bit patterns order like their values.
 #include "common.cuh"
 #include "kernels.h"
@@ -67,9 +69,7 @@ __global__ void __launch_bounds__(kSelChunk) sel_count_kernel(const int32_t* __r
   const int e = u < P ? idx[u] : -1;
   const bool good = u < P && e >= 0 && e < E;
   if (u < P && !good) set_status(status, LRM_ERR_BAD_INDEX);
-  // warp-aggregated: one shared atomic per distinct expert in the warp
-  const unsigned peers = __match_any_sync(0xffffffffu, good ? e : -1);
-  if (good && (threadIdx.x & 31) == __ffs(peers) - 1) atomicAdd(&hist[e], __popc(peers));
+  if (good) atomicAdd(&hist[e], 1);
   __syncthreads();
   for (int e = threadIdx.x; e < E; e += blockDim.x) counts[c * E + e] = hist[e];
 }
@@ -219,10 +219,14 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total, int* sm) {
   return res;
 }
 
+// `direct`: write row_of_pair[u] here.  Otherwise each bucket slot's row (or -1) is written in
+// bucket order over the key it replaces (the slot's key has been read by then, by the same
+// thread) and sel_rows_kernel scatters them: the scattered stores then run on the whole GPU
+// instead of on the CTA of the largest bucket.
 __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
-    const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u,
-    const uint32_t* __restrict__ sorted_key, int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair) {
+    const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u, uint32_t* sorted_key,
+    int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair, int direct) {
   extern __shared__ uint32_t s_dyn[];
   int* hist = reinterpret_cast<int*>(s_dyn);  // [kExpBins]
   uint32_t* s_keys = s_dyn + kExpBins;        // [kExpKeysCap]
@@ -236,18 +240,22 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
   const int keep = keep_arr[e];
   const int base = seg_offsets[e];
   const int32_t* bu = sorted_u + b0;
-  const uint32_t* bk = sorted_key + b0;
+  uint32_t* bk = sorted_key + b0;
 
   if (keep >= load) {
     for (int i = tid; i < load; i += kExpThreads) {
       const int u = bu[i];
       kept_pair[base + i] = u;
-      row_of_pair[u] = base + i;
+      if (direct) row_of_pair[u] = base + i;
+      else bk[i] = (uint32_t)(base + i);
     }
     return;
   }
   if (keep <= 0) {
-    for (int i = tid; i < load; i += kExpThreads) row_of_pair[bu[i]] = -1;
+    for (int i = tid; i < load; i += kExpThreads) {
+      if (direct) row_of_pair[bu[i]] = -1;
+      else bk[i] = 0xffffffffu;
+    }
     return;
   }
 
@@ -300,10 +308,9 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
       for (int q = 0; q < 8; ++q) {
         const int i = i0 + q * kExpThreads + tid;
         const bool in = i < n_src && (src_filtered || (keys[q] & hi_mask) == prefix);
-        const int bin = in ? (int)((keys[q] >> shift) & digit_mask) : -1;
-        // scores cluster in a few bins: aggregate per warp before touching shared memory
-        const unsigned peers = __match_any_sync(0xffffffffu, bin);
-        if (in && lane == __ffs(peers) - 1) atomicAdd(&hist[bin], __popc(peers));
+        // one shared atomic per key: on this GPU that beats aggregating equal bins across the
+        // warp first (__match_any_sync), even though the scores cluster in a few bins
+        if (in) atomicAdd(&hist[(keys[q] >> shift) & digit_mask], 1);
       }
     }
     __syncthreads();
@@ -409,14 +416,11 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     for (int q = 0; q < 8; ++q) {
       const int i = wb + q * 32 + lane;
       if (i < load) {
-        const int u = bu[i];
-        if ((kfm[q] >> lane) & 1u) {
-          const int r = base + pos + __popc(kfm[q] & lt_mask);
-          kept_pair[r] = u;
-          row_of_pair[u] = r;
-        } else {
-          row_of_pair[u] = -1;
-        }
+        const bool kept = (kfm[q] >> lane) & 1u;
+        const int r = kept ? base + pos + __popc(kfm[q] & lt_mask) : -1;
+        if (kept) kept_pair[r] = bu[i];
+        if (direct) row_of_pair[bu[i]] = r;
+        else bk[i] = (uint32_t)r;
       }
       pos += __popc(kfm[q]);
     }
@@ -424,6 +428,20 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     run_kept += tot_kept;
   }
 }
+
+// row_of_pair[sorted_u[i]] = the row that sel_expert_kernel left in slot i (deferred mode).
+__global__ void __launch_bounds__(256) sel_rows_kernel(const int32_t* __restrict__ bucket_start, int E,
+                                                       const int32_t* __restrict__ sorted_u,
+                                                       const uint32_t* __restrict__ slot_row,
+                                                       int32_t* __restrict__ row_of_pair) {
+  const int64_t n = bucket_start[E];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
+    row_of_pair[sorted_u[i]] = (int32_t)slot_row[i];
+}
+
+// From this many pairs on, the rows are scattered by sel_rows_kernel (one launch more; the
+// largest bucket's CTA no longer issues its scattered stores alone).
+constexpr int64_t kDeferRowsMinPairs = 131072;
 
 }  // namespace
 
@@ -445,8 +463,14 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
       cudaFuncSetAttribute(sel_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
       attr_set = true;
     }
+    const bool direct = P < kDeferRowsMinPairs;
     sel_expert_kernel<<<E, kExpThreads, smem, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u,
-                                                  ws.sorted_key, kept_pair, row_of_pair);
+                                                  ws.sorted_key, kept_pair, row_of_pair, direct ? 1 : 0);
+    if (!direct) {
+      const int64_t blocks = (P + 255) / 256;
+      sel_rows_kernel<<<(unsigned)(blocks < 1216 ? blocks : 1216), 256, 0, s>>>(ws.bucket_start, E, ws.sorted_u,
+                                                                               ws.sorted_key, row_of_pair);
+    }
   }
 }
 
