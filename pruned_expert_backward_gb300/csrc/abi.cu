@@ -31,7 +31,7 @@ lrm_status after_launch() {
 
 }  // namespace
 
-size_t gemm_ws_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 1)) + 128 * 4 * (size_t)E; }
+size_t gemm_ws_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 1)) + 128 * 6 * (size_t)E; }
 
 // lrm_grouped_backward's scratch: tile tables and tensor maps, then (only when row_dot is
 // requested) the dphi . phi parts of every row.

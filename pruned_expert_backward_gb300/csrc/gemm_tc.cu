@@ -73,6 +73,16 @@ constexpr int kEpiBytes = 32 * kVmLd * 4;
 // (4 KB, 1024-byte-aligned)
 constexpr int kBoxBytes = 4096;
 static_assert(kBoxBytes <= kEpiBytes, "staging box must fit in the per-warp epilogue region");
+// var-M epilogue through TMA (compacted rows): results leave by TMA stores of 32-row x 32-column
+// bf16 boxes (64-byte swizzle) through per-expert maps whose row extent ends at the segment end,
+// so rows past it are clipped by the hardware; the SwiGLU gate/up tiles arrive by TMA one chunk
+// ahead, into two 4 KB buffers per warp (the launches with a shallower operand pipeline have the
+// room: 8 KB per epilogue warp).
+constexpr int kEpiBytesWide = 8192;
+template <int S>
+__host__ __device__ constexpr int epi_bytes() { return S < kStages ? kEpiBytesWide : kEpiBytes; }
+constexpr int kVmBoxBytes = 2048;  // 32 rows x 64 bytes
+static_assert(kSwigluStages < kStages, "the dphi launch's epilogue needs the wide per-warp buffers");
 constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
@@ -111,6 +121,9 @@ struct TcParams {
   // line instead of being zero-filled).
   int merged_a;  // VK: A
   int merged_b;  // VK and VM: B
+  // VM, compacted rows: epilogue through TMA.  maps_a then holds the per-expert output maps
+  // (dh_c viewed as [rows][2][I], dx_c as [rows][H]), and tmC the gate/up map of h_c ([rows][2][I]).
+  int tma_epi;
 };
 
 // ---------------------------------------------------------------- PTX wrappers -------
@@ -229,6 +242,15 @@ __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(cbar)
       : "memory");
 }
+// TMA load into this CTA's shared memory, completing on this CTA's mbarrier.
+__device__ __forceinline__ void tma_load_3d_cta(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
 // 16-byte cp.async into shared memory; src_bytes < 16 zero-fills the rest (0: nothing is read).
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32_t src_bytes) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes) : "memory");
@@ -256,6 +278,14 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t sr
                : "memory");
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, uint32_t src, int c0, int c1) {
+  asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(src)
+               : "memory");
+  asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 // A tensor map written by another kernel (generic proxy) must be acquired by the tensormap
@@ -368,7 +398,11 @@ __device__ __forceinline__ Tile decode(const TcParams& p, int t, int rank) {
 template <int S>
 __host__ __device__ constexpr uint32_t epi_offset() { return (uint32_t)S * kStageBytes; }
 template <int S>
-__host__ __device__ constexpr uint32_t bar_offset() { return epi_offset<S>() + kEpiWarps * kEpiBytes; }
+__host__ __device__ constexpr uint32_t bar_offset() { return epi_offset<S>() + kEpiWarps * epi_bytes<S>(); }
+// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, gathered[S], then two per epilogue
+// warp for its gate/up buffers
+template <int S>
+__host__ __device__ constexpr int n_barriers() { return 3 * S + 5 + 2 * kEpiWarps; }
 
 // ---------------------------------------------------------------- the kernel ---------
 template <int S>
@@ -379,8 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* epi = smem + epi_offset<S>();
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_offset<S>());
-  // bars: full[S], empty[S], acc_full[2], acc_empty[2], drain, gathered[S]
-  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + 3 * S + 5);
+  uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + n_barriers<S>());
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -406,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acce0, 2 * kEpiWarps);  // leader's: the epilogue warps of both CTAs
     mbar_init(acce0 + 8, 2 * kEpiWarps);
     mbar_init(drain, 1);
+    for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(smem_u32(bars + 3 * S + 5 + i), 1);
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -657,6 +691,136 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     // drain: all MMAs writing this CTA's TMEM complete before it is released
     mbar_wait(drain, 0, abortv, p.status, false);
+  } else if (warp >= 2 && warp < first_extra && p.kind != VK && p.tma_epi) {
+    // ---------------------------------------------------- epilogue, var-M through TMA -------
+    // Warp w reads TMEM lanes 32*(w%4) .. +31 (tile rows q*32 .. +31) and half of the 256 columns,
+    // 32 at a time, one row per lane.  A chunk's 32 x 32 results are packed to bf16 into a
+    // 64-byte-swizzled box (16-byte piece j of row r at j ^ ((r >> 1) & 3)) and leave by one TMA
+    // store per box through the expert's output map, which clips the rows past the segment end.
+    // dphi + SwiGLU: the chunk's gate and up tiles arrive by TMA (issued one chunk ahead, the first
+    // before the accumulator is ready) into the buffer the results then overwrite.
+    const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+    const bool swiglu = p.kind == VM_SWIGLU;
+    uint8_t* wbuf = epi + ew * (swiglu ? epi_bytes<S>() : kBoxBytes);
+    const uint32_t wbuf_s = smem_u32(wbuf);
+    const uint32_t hb0 = smem_u32(bars + 3 * S + 5 + 2 * ew);  // this warp's two gate/up buffer barriers
+    const int swz = (lane >> 1) & 3;
+    uint32_t h_next = 0, h_use = 0, n_st = 0;  // gate/up loads issued / consumed, dx stores issued
+    int last_e = -1;
+    bool ok = true;
+    int lt = 0;
+    for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+      const Tile d = decode(p, t, rank);
+      const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
+      const int row_base = d.row0 + q * 32;
+      const int nrows = d.has_rows ? min(32, d.row_end - row_base) : 0;
+      int nch = 0;  // live 32-column chunks of this warp
+      if (nrows > 0)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (d.n0 + (half * 4 + j) * 32 < p.N) nch = j + 1;
+      const CUtensorMap* omap = p.maps_a + d.e;
+      if (lane == 0 && nch > 0 && d.e != last_e) {
+        tensormap_acquire(omap);
+        last_e = d.e;
+      }
+      // lane 0: the gate and up boxes of chunk c into buffer h_next & 1 (whose previous contents
+      // were last read by a TMA store, so that read completes first)
+      auto issue_h = [&](int c) {
+        const uint32_t b = h_next & 1u, buf = wbuf_s + b * 4096, bar = hb0 + 8 * b;
+        bulk_wait_read_all();
+        mbar_expect_tx(bar, 2 * kVmBoxBytes);
+        tma_load_3d_cta(buf, &tmC, d.n0 + c * 32, 0, row_base, bar);
+        tma_load_3d_cta(buf + kVmBoxBytes, &tmC, d.n0 + c * 32, 1, row_base, bar);
+      };
+      if (swiglu && nch > 0) {
+        if (lane == 0) issue_h(half * 4);
+        ++h_next;
+      }
+      if (!mbar_wait(accf0 + 8 * acc, acc_ph, abortv, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * kBN + ((uint32_t)(q * 32) << 16);
+      // dphi . phi over this lane's row and the warp's columns, in four parts (one per 8-column
+      // group of a chunk) added as (p0 + p1) + (p2 + p3): the same order as the other epilogue,
+      // so that both row deliveries give bit-identical results
+      float rp[4] = {0.f, 0.f, 0.f, 0.f};
+      for (int j = 0; j < nch; ++j) {
+        const int c = half * 4 + j, n = d.n0 + c * 32;
+        if (swiglu && j + 1 < nch) {
+          if (lane == 0) issue_h(c + 1);
+          ++h_next;
+        }
+        uint32_t v[32];
+        tmem_ld32(tbase + c * 32, v);
+        if (swiglu) {
+          const uint32_t g = h_use++;
+          if (!__all_sync(0xffffffffu, mbar_wait(hb0 + 8 * (g & 1u), (g >> 1) & 1u, abortv, p.status))) {
+            ok = false;
+            break;
+          }
+          uint8_t* hbuf = wbuf + (g & 1u) * 4096;
+          uint8_t* grow = hbuf + lane * 64;
+          uint8_t* urow = grow + kVmBoxBytes;
+          uint4 gq[4], uq[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            gq[jj] = *reinterpret_cast<const uint4*>(grow + ((jj ^ swz) << 4));
+            uq[jj] = *reinterpret_cast<const uint4*>(urow + ((jj ^ swz) << 4));
+          }
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float gate[8], up[8], dg[8], du[8];
+            unpack(gq[jj], gate);
+            unpack(uq[jj], up);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const float dphi = __uint_as_float(v[8 * jj + i]);
+              const float sg = 1.f / (1.f + __expf(-gate[i]));
+              dg[i] = dphi * up[i] * sg * (1.f + gate[i] * (1.f - sg));
+              du[i] = dphi * gate[i] * sg;
+              if (n + 8 * jj + i < p.N) rp[jj] = fmaf(du[i], up[i], rp[jj]);
+            }
+            *reinterpret_cast<uint4*>(grow + ((jj ^ swz) << 4)) = pack(dg);
+            *reinterpret_cast<uint4*>(urow + ((jj ^ swz) << 4)) = pack(du);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_3d(omap, smem_u32(hbuf), n, 0, row_base);
+            tma_store_3d(omap, smem_u32(hbuf) + kVmBoxBytes, n, 1, row_base);
+          }
+        } else {
+          uint8_t* box = wbuf + (n_st & 1u) * kVmBoxBytes;
+          ++n_st;
+          if (lane == 0) bulk_wait_read_le1();  // the store before last (this box's) has read it
+          __syncwarp();
+          uint8_t* row = box + lane * 64;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = __uint_as_float(v[8 * jj + i]);
+            *reinterpret_cast<uint4*>(row + ((jj ^ swz) << 4)) = pack(f);
+          }
+          asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+          __syncwarp();
+          if (lane == 0) tma_store_2d(omap, smem_u32(box), n, row_base);
+        }
+      }
+      if (!ok) break;
+      if (swiglu && p.dot_part != nullptr && nch > 0 && lane < nrows)
+        p.dot_part[(int64_t)(row_base + lane) * p.n_part + d.n0 / 128 + half] = (rp[0] + rp[1]) + (rp[2] + rp[3]);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_lead + 8 * acc);
+    }
+    // no gate/up load may land, and no store may read, after the CTA has exited
+    for (uint32_t g = h_use; g < h_next; ++g)
+      mbar_wait(hb0 + 8 * (g & 1u), (g >> 1) & 1u, abortv, p.status, false);
+    if (lane == 0) bulk_wait_all();
   } else if (warp >= 2 && warp < first_extra) {
     // ------------------------------------------------------------ epilogue -----------
     // Warp w may read TMEM lanes 32*(w%4) .. +31 (tile rows q*32 .. q*32+31); the two warps
@@ -665,7 +829,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // stores (and the SwiGLU h_c loads) are coalesced; var-M rows are masked at the segment end.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     const int sub = lane >> 2, piece = lane & 3;  // var-M stores: lane owns 8 columns of one row
-    float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : kEpiBytes));
+    float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : epi_bytes<S>()));
     int lt = 0;
     for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
       const Tile d = decode(p, t, rank);
@@ -813,9 +977,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Tile tables from seg_offsets: plan[0..E] = exclusive prefix of ceil(R_e / 256) (var-M pair tiles),
 // plan[E+1 .. 2E] = experts ordered by R_e descending, ties by expert id (var-K, longest first).
-// maps[j][e] = template j with its row extent cut at seg_offsets[e+1] (var-K operands).
+// maps[j][e] = template j with its row extent cut at seg_offsets[e+1] (var-K operands, var-M outputs).
+// Templates 0-3: var-K operands (row extent is dimension 1); 4: dh_c as [rows][2][I] (rows are
+// dimension 2); 5: dx_c as [rows][H] (dimension 1).
+constexpr int kMapSets = 6;
 struct MapTemplates {
-  CUtensorMap t[4];
+  CUtensorMap t[kMapSets];
 };
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict__ seg, int E,
                                                        int32_t* __restrict__ plan, CUtensorMap* __restrict__ maps,
@@ -858,16 +1025,22 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
     }
     plan[E + 1 + rank] = e;
     const uint32_t rows_end = (uint32_t)max(1, seg[e + 1]);
-    for (int j = 0; j < 4; ++j) {
+    for (int j = 0; j < kMapSets; ++j) {
       CUtensorMap* dst = maps + j * E + e;
       const uint4* src = reinterpret_cast<const uint4*>(&tpl.t[j]);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
       for (int w = 0; w < 8; ++w) d4[w] = src[w];
-      asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
-                       reinterpret_cast<uint64_t>(dst)),
-                   "r"(rows_end)
-                   : "memory");
+      if (j == 4)
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 2, %1;" ::"l"(
+                         reinterpret_cast<uint64_t>(dst)),
+                     "r"(rows_end)
+                     : "memory");
+      else
+        asm volatile("tensormap.replace.tile.global_dim.global.b1024.b32 [%0], 1, %1;" ::"l"(
+                         reinterpret_cast<uint64_t>(dst)),
+                     "r"(rows_end)
+                     : "memory");
     }
     asm volatile("fence.proxy.tensormap::generic.release.gpu;" ::: "memory");
   }
@@ -948,6 +1121,27 @@ bool make_map_blocks_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
+// bf16 [rows][2][I] (gate / up halves of a row, e.g. h_c or dh_c) with a {32, 1, 32} box,
+// 64-byte swizzle: one box is 32 columns of one half for 32 rows.
+bool make_map_halves(CUtensorMap* m, const void* base, uint64_t rows, uint64_t I) {
+  const cuuint64_t dims[3] = {I, 2, rows};
+  const cuuint64_t strides[2] = {I * 2, I * 4};
+  const cuuint32_t box[3] = {32, 1, 32};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// bf16 [rows][cols] with a {32, 32} box, 64-byte swizzle.
+bool make_map_rows32(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols) {
+  const cuuint64_t dims[2] = {cols, rows};
+  const cuuint64_t strides[1] = {cols * 2};
+  const cuuint32_t box[2] = {32, 32};
+  const cuuint32_t estr[2] = {1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 // Column counts whose 64-column blocks may share one box (see TcParams::merged_a).
 bool mergeable(uint64_t cols) { return cols % 64 == 0 && cols >= 128; }
 
@@ -963,7 +1157,7 @@ bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t
 }
 
 template <int S>
-size_t smem_bytes() { return 1024 + bar_offset<S>() + (3 * S + 5) * 8 + 8; }
+size_t smem_bytes() { return 1024 + bar_offset<S>() + n_barriers<S>() * 8 + 8; }
 
 int sm_count() {
   static int n = 0;
@@ -1053,6 +1247,10 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (!vk_map(0, g.dy_c, H) || !vk_map(1, gather ? g.dy_c : g.phi_c, I) || !vk_map(2, g.dh_c, 2 * I) ||
       !vk_map(3, gather ? g.dy_c : g.x_c, H))
     return LRM_ERR_CUDA;
+  // var-M outputs (per-expert copies clip the rows past the segment end)
+  if (!make_map_halves(&tpl.t[4], g.dh_c, rows, I) || !make_map_rows32(&tpl.t[5], g.dx_c, rows, H))
+    return LRM_ERR_CUDA;
+  const int tma_epi = gather ? 0 : 1;  // compacted rows: var-M epilogue through TMA
   // var-M weight maps: [E, K, N], blocked the same way where N allows
   auto vm_map = [&](CUtensorMap* m, const void* base, uint64_t K, uint64_t N, int* merged_b) {
     *merged_b = mergeable(N) && make_map_blocks_3d(m, base, E, K, N);
@@ -1069,9 +1267,11 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (!make_map_2d(&mA, g.dy_c, rows, H, kBM) || !vm_map(&mB, g.w_down, H, I, &vm_merged)) return LRM_ERR_CUDA;
   using B16 = const __nv_bfloat16*;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
-             (B16)g.h_c, g.status, nullptr, nullptr, g.dot_part, (I + 127) / 128,
-             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I, 0, vm_merged};
-  if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
+             (B16)g.h_c, g.status, maps + 4 * E, nullptr, g.dot_part, (I + 127) / 128,
+             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I, 0, vm_merged, tma_epi};
+  CUtensorMap mH = mA;  // gate/up tiles of h_c for the TMA epilogue
+  if (tma_epi && !make_map_halves(&mH, g.h_c, rows, I)) return LRM_ERR_CUDA;
+  if ((st = launch_one(mA, mB, mH, p, vm_bound * p.nN, s))) return st;
   if (g.row_dot != nullptr) launch_row_dot(g.dot_part, p.n_part, g.seg_offsets, E, g.cap, g.row_dot, s);
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
@@ -1094,8 +1294,9 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !vm_map(&mB, g.w_gate_up, 2 * I, H, &vm_merged))
     return LRM_ERR_CUDA;
   p = TcParams{VM_STORE, E, 0, H, 2 * I, 0, (H + kBN - 1) / kBN, g.seg_offsets, plan, g.dx_c, nullptr,
-               g.status, nullptr, nullptr};
+               g.status, maps + 5 * E, nullptr};
   p.merged_b = vm_merged;
+  p.tma_epi = tma_epi;
   if ((st = launch_one(mA, mB, mA, p, vm_bound * p.nN, s))) return st;
   return LRM_OK;
 }

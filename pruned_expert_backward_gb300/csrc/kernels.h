@@ -23,11 +23,11 @@ struct SelectWs {
   int64_t n_chunks;
 };
 
-// Scratch of the tensor-core grouped GEMMs: tile tables, then 4*E per-expert TMA tensor maps
+// Scratch of the tensor-core grouped GEMMs: tile tables, then 6*E per-expert TMA tensor maps
 // (128 bytes each, 128-byte aligned) built on the device from seg_offsets.
 struct GemmWs {
   int32_t* plan;  // [2E+1]
-  void* maps;     // [4][E] CUtensorMap
+  void* maps;     // [6][E] CUtensorMap
 };
 size_t gemm_ws_bytes(int32_t E);
 
