@@ -28,6 +28,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
                                                       const T* __restrict__ phi, int k, int H, int I, int64_t cap,
                                                       T* __restrict__ dy_c, T* __restrict__ x_c, T* __restrict__ h_c,
                                                       T* __restrict__ phi_c) {
+  chain_wait();
   constexpr int VN = VecTraits<T>::N;
   __shared__ int64_t s_row[LRM_MAX_TOPK];
   __shared__ float s_alpha[LRM_MAX_TOPK];
@@ -100,6 +101,7 @@ template <typename T>
 __global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
                                                          const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
                                                          T* __restrict__ dx) {
+  chain_wait();
   constexpr int VN = VecTraits<T>::N;
   constexpr int B = kScatterLoads;
   __shared__ int2 s_item[kScatterTok * LRM_MAX_TOPK];  // (token within the CTA, compacted row)
@@ -165,13 +167,12 @@ void launch_compact(const int32_t* row_of_pair, const float* alpha, const void* 
   if (T == 0) return;
   if (dt == LRM_BF16) {
     using B = __nv_bfloat16;
-    compact_kernel<B><<<(unsigned)T, 256, 0, s>>>(row_of_pair, alpha, (const B*)g, (const B*)x, (const B*)h,
-                                                  (const B*)phi, k, H, I, cap, (B*)dy_c, (B*)x_c, (B*)h_c,
-                                                  (B*)phi_c);
+    launch_chained(compact_kernel<B>, dim3((unsigned)T), dim3(256), 0, s, row_of_pair, alpha, (const B*)g,
+                   (const B*)x, (const B*)h, (const B*)phi, k, H, I, cap, (B*)dy_c, (B*)x_c, (B*)h_c, (B*)phi_c);
   } else {
-    compact_kernel<float><<<(unsigned)T, 256, 0, s>>>(row_of_pair, alpha, (const float*)g, (const float*)x,
-                                                      (const float*)h, (const float*)phi, k, H, I, cap,
-                                                      (float*)dy_c, (float*)x_c, (float*)h_c, (float*)phi_c);
+    launch_chained(compact_kernel<float>, dim3((unsigned)T), dim3(256), 0, s, row_of_pair, alpha, (const float*)g,
+                   (const float*)x, (const float*)h, (const float*)phi, k, H, I, cap, (float*)dy_c, (float*)x_c,
+                   (float*)h_c, (float*)phi_c);
   }
 }
 
@@ -183,10 +184,11 @@ void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, 
   if (threads > 256) threads = 256;
   const unsigned blocks = (unsigned)((T + kScatterTok - 1) / kScatterTok);
   if (dt == LRM_BF16)
-    scatter_dx_kernel<__nv_bfloat16><<<blocks, threads, 0, s>>>(row_of_pair, (const __nv_bfloat16*)dx_c, T, k, H,
-                                                                (__nv_bfloat16*)dx);
+    launch_chained(scatter_dx_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, row_of_pair,
+                   (const __nv_bfloat16*)dx_c, T, k, H, (__nv_bfloat16*)dx);
   else
-    scatter_dx_kernel<float><<<blocks, threads, 0, s>>>(row_of_pair, (const float*)dx_c, T, k, H, (float*)dx);
+    launch_chained(scatter_dx_kernel<float>, dim3(blocks), dim3(threads), 0, s, row_of_pair, (const float*)dx_c, T,
+                   k, H, (float*)dx);
 }
 
 }  // namespace lrm

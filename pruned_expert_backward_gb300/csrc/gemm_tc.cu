@@ -449,6 +449,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync_all();  // both CTAs' barriers exist before any remote operation targets them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_holder;
+  // the set-up above touches no global memory, so it overlaps the end of the previous kernel
+  chain_wait();
   const int n_tiles = total_tiles(p);
   volatile int* abortv = abort_flag;
   const uint32_t full_lead = cluster_addr(full0, 0), acce_lead = cluster_addr(acce0, 0);
@@ -987,6 +989,7 @@ struct MapTemplates {
 __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict__ seg, int E,
                                                        int32_t* __restrict__ plan, CUtensorMap* __restrict__ maps,
                                                        const __grid_constant__ MapTemplates tpl) {
+  chain_wait();
   __shared__ int s_r[LRM_MAX_EXPERTS];
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
@@ -1190,7 +1193,9 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
     attr_set = true;
   }
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see chain_wait()
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
@@ -1200,7 +1205,7 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
   cfg.dynamicSmemBytes = smem;
   cfg.stream = s;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
   static int max_pairs = 0;
   if (max_pairs == 0) {
     cfg.gridDim = dim3(2 * sm_count() / 2);
@@ -1208,6 +1213,7 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
     if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_kernel<S>, &cfg) != cudaSuccess || n <= 0) n = sm_count() / 2;
     max_pairs = n;
   }
+  cfg.numAttrs = 2;
   const int64_t pairs = tiles_bound < max_pairs ? tiles_bound : max_pairs;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
   if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel<S>, a, b, c, p) != cudaSuccess) return LRM_ERR_CUDA;
@@ -1256,7 +1262,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
     *merged_b = mergeable(N) && make_map_blocks_3d(m, base, E, K, N);
     return *merged_b || make_map_3d(m, base, E, K, N);
   };
-  tc_plan_kernel<<<1, 1024, 0, s>>>(g.seg_offsets, E, plan, maps, tpl);
+  launch_chained(tc_plan_kernel, dim3(1), dim3(1024), 0, s, g.seg_offsets, E, plan, maps, tpl);
   if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
 
   CUtensorMap mA, mB;

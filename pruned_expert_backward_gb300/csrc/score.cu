@@ -54,6 +54,7 @@ __global__ void __launch_bounds__(256) score_kernel(const float* __restrict__ al
                                                    float* __restrict__ scores, int32_t* status) {
   // One warp per token: ||g_t||^2 once, then the token's k contiguous phi rows two at a time.
   // GV / PV bound the 16-byte vectors per lane of a g row / phi row (0 = unbounded, looped).
+  chain_wait();
   constexpr int VN = VecTraits<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -98,6 +99,7 @@ template <typename T, int GV, int PV, int MAXK>
 __global__ void __launch_bounds__(128) score_onepass_kernel(const float* __restrict__ alpha, const T* __restrict__ g,
                                                            const T* __restrict__ phi, int64_t n_tok, int k, int H,
                                                            int I, float* __restrict__ scores, int32_t* status) {
+  chain_wait();
   constexpr int VN = VecTraits<T>::N;
   const int lane = threadIdx.x & 31;
   const int64_t t = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -237,14 +239,14 @@ void launch_score(const float* alpha, const void* g, const void* phi, int64_t T,
   const int gv = (H / vn + 31) / 32, pv = (I / vn + 31) / 32;  // vectors per lane of a g / phi row
   if (dt == LRM_BF16 && gv <= 8 && pv <= 3 && k <= 8) {
     using B = __nv_bfloat16;
-    score_onepass_kernel<B, 8, 3, 8><<<(unsigned)((T + 3) / 4), 128, 0, s>>>(alpha, (const B*)g, (const B*)phi, T, k,
-                                                                          H, I, scores, status);
+    launch_chained(score_onepass_kernel<B, 8, 3, 8>, dim3((unsigned)((T + 3) / 4)), dim3(128), 0, s, alpha,
+                   (const B*)g, (const B*)phi, T, k, H, I, scores, status);
     return;
   }
   const bool fits = gv <= 16 && pv <= 6;
 #define LRM_SCORE_LAUNCH(TYPE, GV, PV)                                                                 \
-  score_kernel<TYPE, GV, PV><<<(unsigned)blocks, 256, 0, s>>>(alpha, (const TYPE*)g, (const TYPE*)phi, T, k, H, \
-                                                            I, scores, status)
+  launch_chained(score_kernel<TYPE, GV, PV>, dim3((unsigned)blocks), dim3(256), 0, s, alpha, (const TYPE*)g, \
+                 (const TYPE*)phi, T, k, H, I, scores, status)
   if (dt == LRM_BF16) {
     if (fits) LRM_SCORE_LAUNCH(__nv_bfloat16, 16, 6); else LRM_SCORE_LAUNCH(__nv_bfloat16, 0, 0);
   } else {

@@ -61,6 +61,7 @@ __device__ __forceinline__ int block_excl_scan(int v, int* total, int* sm) {
 
 __global__ void __launch_bounds__(kSelChunk) sel_count_kernel(const int32_t* __restrict__ idx, int64_t P, int E,
                                                               int32_t* __restrict__ counts, int32_t* status) {
+  chain_wait();
   extern __shared__ int hist[];  // [E]
   for (int e = threadIdx.x; e < E; e += blockDim.x) hist[e] = 0;
   __syncthreads();
@@ -77,6 +78,7 @@ __global__ void __launch_bounds__(kSelChunk) sel_count_kernel(const int32_t* __r
 // One CTA per expert: exclusive scan down the expert's column of chunk counts.
 __global__ void __launch_bounds__(1024) sel_colscan_kernel(int32_t* __restrict__ counts, int64_t n_chunks, int E,
                                                            int32_t* __restrict__ loads) {
+  chain_wait();
   __shared__ int sm[33];
   __shared__ int s_run;
   const int e = blockIdx.x;
@@ -101,6 +103,7 @@ __global__ void __launch_bounds__(kSelChunk) sel_bucket_kernel(
     int64_t cap, int32_t* __restrict__ bucket_start, int32_t* __restrict__ keep, int32_t* __restrict__ seg_offsets,
     int32_t* __restrict__ sorted_u, uint32_t* __restrict__ sorted_key, int32_t* __restrict__ row_of_pair,
     int32_t* status) {
+  chain_wait();
   constexpr int kWarps = kSelChunk / 32;
   extern __shared__ int sh[];
   int* s_base = sh;              // [E]  this chunk's first slot of each expert
@@ -227,6 +230,7 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
     const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u, uint32_t* sorted_key,
     int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair, int direct) {
+  chain_wait();
   extern __shared__ uint32_t s_dyn[];
   int* hist = reinterpret_cast<int*>(s_dyn);  // [kExpBins]
   uint32_t* s_keys = s_dyn + kExpBins;        // [kExpKeysCap]
@@ -434,6 +438,7 @@ __global__ void __launch_bounds__(256) sel_rows_kernel(const int32_t* __restrict
                                                        const int32_t* __restrict__ sorted_u,
                                                        const uint32_t* __restrict__ slot_row,
                                                        int32_t* __restrict__ row_of_pair) {
+  chain_wait();
   const int64_t n = bucket_start[E];
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
     row_of_pair[sorted_u[i]] = (int32_t)slot_row[i];
@@ -450,12 +455,13 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
                    int32_t* status, cudaStream_t s) {
   const int64_t nc = ws.n_chunks;
   if (nc > 0)
-    sel_count_kernel<<<(unsigned)nc, kSelChunk, E * sizeof(int), s>>>(topk_idx, P, E, ws.counts, status);
-  sel_colscan_kernel<<<E, 1024, 0, s>>>(ws.counts, nc, E, ws.loads);
+    launch_chained(sel_count_kernel, dim3((unsigned)nc), dim3(kSelChunk), E * sizeof(int), s, topk_idx, P, E,
+                   ws.counts, status);
+  launch_chained(sel_colscan_kernel, dim3(E), dim3(1024), 0, s, ws.counts, nc, E, ws.loads);
   const size_t bsmem = (size_t)(2 + kSelChunk / 32) * E * sizeof(int);
-  sel_bucket_kernel<<<nc > 0 ? (unsigned)nc : 1u, kSelChunk, bsmem, s>>>(
-      topk_idx, scores, P, E, nc, ws.counts, ws.loads, quotas, cap, ws.bucket_start, ws.keep, seg_offsets,
-      ws.sorted_u, ws.sorted_key, row_of_pair, status);
+  launch_chained(sel_bucket_kernel, dim3(nc > 0 ? (unsigned)nc : 1u), dim3(kSelChunk), bsmem, s, topk_idx, scores, P,
+                 E, nc, (const int32_t*)ws.counts, (const int32_t*)ws.loads, quotas, cap, ws.bucket_start, ws.keep,
+                 seg_offsets, ws.sorted_u, ws.sorted_key, row_of_pair, status);
   if (P > 0) {
     static bool attr_set = false;
     const int smem = (int)kExpSmemBytes;
@@ -464,12 +470,14 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
       attr_set = true;
     }
     const bool direct = P < kDeferRowsMinPairs;
-    sel_expert_kernel<<<E, kExpThreads, smem, s>>>(ws.bucket_start, ws.keep, seg_offsets, ws.sorted_u,
-                                                  ws.sorted_key, kept_pair, row_of_pair, direct ? 1 : 0);
+    launch_chained(sel_expert_kernel, dim3(E), dim3(kExpThreads), (size_t)smem, s, (const int32_t*)ws.bucket_start,
+                   (const int32_t*)ws.keep, (const int32_t*)seg_offsets, (const int32_t*)ws.sorted_u, ws.sorted_key,
+                   kept_pair, row_of_pair, direct ? 1 : 0);
     if (!direct) {
       const int64_t blocks = (P + 255) / 256;
-      sel_rows_kernel<<<(unsigned)(blocks < 1216 ? blocks : 1216), 256, 0, s>>>(ws.bucket_start, E, ws.sorted_u,
-                                                                               ws.sorted_key, row_of_pair);
+      launch_chained(sel_rows_kernel, dim3((unsigned)(blocks < 1216 ? blocks : 1216)), dim3(256), 0, s,
+                     (const int32_t*)ws.bucket_start, E, (const int32_t*)ws.sorted_u, (const uint32_t*)ws.sorted_key,
+                     row_of_pair);
     }
   }
 }
