@@ -1027,9 +1027,13 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
       rank += (rj > r) || (rj == r && j < e);
     }
     plan[E + 1 + rank] = e;
-    const uint32_t rows_end = (uint32_t)max(1, seg[e + 1]);
-    for (int j = 0; j < kMapSets; ++j) {
-      CUtensorMap* dst = maps + j * E + e;
+  }
+  // one (template, expert) map per thread
+  for (int i = threadIdx.x; i < kMapSets * E; i += blockDim.x) {
+    const int j = i / E, ee = i - j * E;
+    const uint32_t rows_end = (uint32_t)max(1, seg[ee + 1]);
+    {
+      CUtensorMap* dst = maps + j * E + ee;
       const uint4* src = reinterpret_cast<const uint4*>(&tpl.t[j]);
       uint4* d4 = reinterpret_cast<uint4*>(dst);
 #pragma unroll
