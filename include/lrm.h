@@ -32,6 +32,13 @@
  *    The caller reads it whenever it chooses; the library never does.
  *  - Limits: 1 <= E <= LRM_MAX_EXPERTS, 1 <= k <= LRM_MAX_TOPK, P <= INT32_MAX,
  *    H and I positive multiples of 8.
+ *  - The kernels of lrm_score, lrm_select, lrm_select_static, lrm_compact,
+ *    lrm_grouped_backward (tensor-core path) and lrm_scatter_dx use programmatic dependent launch: each waits (griddepcontrol.wait) for the
+ *    work queued before it on the stream to complete before it touches memory, and lets the
+ *    next launch on the stream start early.  Ordinary stream order therefore holds for every
+ *    caller; a caller kernel that is itself launched with programmatic stream serialization
+ *    right after one of these calls must execute griddepcontrol.wait (or
+ *    cudaGridDependencySynchronize) before it reads their outputs.
  */
 #ifndef LRM_H
 #define LRM_H
