@@ -84,6 +84,9 @@ SMALL = [
     W.small_workload("bf16_qwen_shape_small_T", 700, 2048, 768, 128, 8),
     W.small_workload("bf16_zipf15_cap", 2048, 512, 256, 32, 8, zipf_s=1.5, quota=("cap", 300)),
     W.small_workload("bf16_drop30", 1536, 256, 136, 24, 6, quota=("ratio", 7, 10)),
+    # H = 200 and I = 96: the last 32-column dX_c store box is clipped by its map, and neither weight
+    # map's column count allows one box per 128-column half
+    W.small_workload("bf16_h_ragged", 800, 200, 96, 12, 4),
     # T*k = 131072 pairs: selection leaves the rows in bucket order and scatters row_of_pair in a
     # launch of its own (the path of the large workloads), on shapes the oracle checks in full
     W.small_workload("bf16_deferred_rows", 16384, 64, 64, 64, 8),
