@@ -18,18 +18,21 @@
 // tcgen05.mma.cta_group::2, which computes a 256 x 256 tile from both CTAs' shared memory
 // (each CTA stages its own 128 rows of A and its own 128 columns of B) into both CTAs' TMEM
 // (128 rows each).  Per SM that is 32 KB of operands per 64-deep K slice instead of 48 KB
-// for a 128 x 256 single-SM tile, and 6 stages fit in shared memory.
+// for a 128 x 256 single-SM tile, and 6 stages fit in shared memory (5 for the dphi launch,
+// whose epilogue needs room for its gate/up tiles).
 // CTA layout (320 threads): warp 0 issues TMA loads (both CTAs; they complete on the
 // leader's full barrier), warp 1 owns TMEM (allocated collectively by the pair) and, in the
 // leader, issues the MMAs from one thread; warps 2-9 drain this CTA's accumulator rows
-// (tcgen05.ld; two warps per 32-row TMEM quarter, each taking half of the columns).  Two
-// 256-column fp32 accumulators in TMEM let the epilogue of one tile overlap the MMAs of the
-// next; both CTAs' epilogues release an accumulator on the leader's barrier.
+// (tcgen05.ld; two warps per 32-row TMEM quarter, each taking half of the columns) and write
+// them out through TMA stores.  Two 256-column fp32 accumulators in TMEM let the epilogue of
+// one tile overlap the MMAs of the next; both CTAs' epilogues release an accumulator on the
+// leader's barrier.
 //
 // Shared-memory operand layouts are the 128-byte-swizzled canonical forms:
 //   K-major  (rows of 64 K-elements = 128 B): SBO = 1024 B between 8-row groups;
 //   MN-major (lines of 64 MN-elements = 128 B, one line per K index): LBO = 8192 B between
-//            64-wide MN blocks (one TMA box each), SBO = 1024 B between 8-line K groups.
+//            64-wide MN blocks, SBO = 1024 B between 8-line K groups; both blocks of a CTA's
+//            128 columns come in one TMA box where the column count allows (see merged_a).
 // In the var-K problems a K slice that runs past the end of a segment would pick up the
 // next expert's rows.  The plan kernel therefore writes, per expert, copies of the operand
 // tensor maps whose row extent ends at that expert's segment end (tensormap.replace on a
@@ -140,9 +143,6 @@ __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -825,10 +825,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) bulk_wait_all();
   } else if (warp >= 2 && warp < first_extra) {
     // ------------------------------------------------------------ epilogue -----------
+    // var-K (fp32 dW through TMA stores) and var-M of the compaction-free variant, whose gate/up
+    // rows are named by kept_pair and so cannot come as TMA tiles.
     // Warp w may read TMEM lanes 32*(w%4) .. +31 (tile rows q*32 .. q*32+31); the two warps
     // of a quarter split the eight 32-column chunks.  Each chunk is read row-per-thread
-    // (tcgen05.ld 32x32b), staged in shared memory and written back row-contiguous, so global
-    // stores (and the SwiGLU h_c loads) are coalesced; var-M rows are masked at the segment end.
+    // (tcgen05.ld 32x32b); var-M chunks are staged in shared memory and written back
+    // row-contiguous, so global stores (and the SwiGLU gate/up loads) are coalesced, masked at
+    // the segment end.
     const int ew = warp - 2, q = warp & 3, half = ew >> 2;
     const int sub = lane >> 2, piece = lane & 3;  // var-M stores: lane owns 8 columns of one row
     float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : epi_bytes<S>()));

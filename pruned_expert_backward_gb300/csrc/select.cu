@@ -4,7 +4,7 @@
 // LRM": inside each expert's quota the highest-scoring pairs are kept.  Equal scores go to
 // the smaller pair index u; inside a segment the kept pairs are listed in u order.
 //
-// Four launches, all deterministic:
+// Four launches (five from 131072 pairs on), all deterministic:
 //  1. count:   one CTA per chunk of kSelChunk consecutive pairs counts the chunk's experts.
 //  2. scan:    one CTA per expert: exclusive scan of that expert's chunk counts (bucket
 //              bases inside the expert's bucket) and its load.

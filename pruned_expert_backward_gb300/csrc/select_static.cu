@@ -4,7 +4,7 @@
 // framework that owns every device buffer and passes its plugins only their inputs and
 // outputs, or a process whose device memory is reserved up front by a pool allocator, where
 // a cudaMalloc would fail or break the pool's accounting.  For them this entry point runs
-// the same four selection kernels as lrm_select, with their scratch in a fixed array that
+// the same selection kernels as lrm_select, with their scratch in a fixed array that
 // is part of the library image on every GPU that loads it (about 12 MB, held until exit).
 //
 // Set-up: the first call on a device (with that device current) looks up the array's
