@@ -95,6 +95,25 @@ __device__ __forceinline__ void chain_wait() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// One-time set-up that belongs to a device (kernel attributes, occupancy, SM counts) is kept
+// per device: a process may drive several GPUs.
+constexpr int kDeviceSlots = 64;
+inline int current_device_slot() {
+  int d = -1;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kDeviceSlots ? d : -1;
+}
+// Allows `Kernel` `bytes` of dynamic shared memory on the current device (once per device).
+template <auto Kernel>
+inline cudaError_t ensure_max_smem(int bytes) {
+  static bool done[kDeviceSlots] = {};
+  const int d = current_device_slot();
+  if (d < 0) return cudaErrorInvalidDevice;
+  if (done[d]) return cudaSuccess;
+  const cudaError_t e = cudaFuncSetAttribute(Kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) done[d] = true;
+  return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
                                   Args&&... args) {

@@ -1170,12 +1170,15 @@ template <int S>
 size_t smem_bytes() { return 1024 + bar_offset<S>() + n_barriers<S>() * 8 + 8; }
 
 int sm_count() {
-  static int n = 0;
+  static int count[kDeviceSlots] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  const int d = current_device_slot();
+  int n = d >= 0 ? count[d] : 0;
   if (n == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
     if (n <= 0) n = 1;
+    if (d >= 0) count[d] = n;
   }
   return n;
 }
@@ -1192,13 +1195,7 @@ template <int S>
 lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                          int64_t tiles_bound, cudaStream_t s) {
   const size_t smem = smem_bytes<S>();
-  static bool attr_set = false;
-  if (!attr_set) {
-    if (cudaFuncSetAttribute(tc_grouped_kernel<S>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return LRM_ERR_CUDA;
-    attr_set = true;
-  }
+  if (ensure_max_smem<tc_grouped_kernel<S>>((int)smem) != cudaSuccess) return LRM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see chain_wait()
@@ -1213,12 +1210,15 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;  // the occupancy query sees the cluster shape only
-  static int max_pairs = 0;
+  static int max_pairs_dev[kDeviceSlots] = {};  // resident CTA pairs, per device
+  const int dslot = current_device_slot();
+  int max_pairs = dslot >= 0 ? max_pairs_dev[dslot] : 0;
   if (max_pairs == 0) {
     cfg.gridDim = dim3(2 * sm_count() / 2);
     int n = 0;
     if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_kernel<S>, &cfg) != cudaSuccess || n <= 0) n = sm_count() / 2;
     max_pairs = n;
+    if (dslot >= 0) max_pairs_dev[dslot] = n;
   }
   cfg.numAttrs = 2;
   const int64_t pairs = tiles_bound < max_pairs ? tiles_bound : max_pairs;

@@ -463,12 +463,8 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
                  E, nc, (const int32_t*)ws.counts, (const int32_t*)ws.loads, quotas, cap, ws.bucket_start, ws.keep,
                  seg_offsets, ws.sorted_u, ws.sorted_key, row_of_pair, status);
   if (P > 0) {
-    static bool attr_set = false;
     const int smem = (int)kExpSmemBytes;
-    if (!attr_set) {
-      cudaFuncSetAttribute(sel_expert_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-      attr_set = true;
-    }
+    ensure_max_smem<sel_expert_kernel>(smem);  // a failure surfaces as the launch's error
     const bool direct = P < kDeferRowsMinPairs;
     launch_chained(sel_expert_kernel, dim3(E), dim3(kExpThreads), (size_t)smem, s, (const int32_t*)ws.bucket_start,
                    (const int32_t*)ws.keep, (const int32_t*)seg_offsets, (const int32_t*)ws.sorted_u, ws.sorted_key,
