@@ -3,8 +3,10 @@
 
 One step = one pass of the whole hot path (score -> select -> compact -> grouped SwiGLU
 expert backward -> scatter dX) over one batch of seeded synthetic input that is already
-resident in HBM.  Default workload: the Qwen3-30B-A3B-shaped layer, T=8192, H=2048,
-I=768, E=128, top-8, bf16, drop 20 % (quota = ceil(0.8 * load)).
+resident in HBM.  Default workload: the largest single-GPU configuration, the
+GLM4.5-106B-A12B-shaped routed-expert layer at the articles' per-GPU batch (sequence
+8192 x microbatch 4): T=32768, H=4096, I=1408, E=128, top-8, bf16, drop 20 %
+(quota = ceil(0.8 * load)).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
        [--workload NAME] [--no-cpu-baseline] [--no-extras]
@@ -148,15 +150,17 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ traffic record --------
-def recorded_traffic(kernel_stage):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the current
-    source of that kernel (the summary stores a hash of the kernel's source file)."""
+def recorded_traffic(kernel_stage, workload):
+    """DRAM bytes per call of a stage from the committed ncu record, if one was taken on this
+    workload and on the current source of that kernel (the record stores a hash of the kernel's
+    source file).  None otherwise: a record of another workload or of older code says nothing
+    about this run."""
     path = os.path.join(ROOT, "profiles", "traffic.txt")
     if not os.path.exists(path):
         return None
     for line in open(path):
         m = re.match(r"\s*stage=(\S+)\s+workload=(\S+)\s+source=(\S+)\s+sha=(\S+)\s+dram_bytes=(\d+)", line)
-        if not m or m.group(1) != kernel_stage:
+        if not m or m.group(1) != kernel_stage or m.group(2) != workload:
             continue
         src = os.path.join(ROOT, m.group(3))
         if not os.path.exists(src):
@@ -168,22 +172,105 @@ def recorded_traffic(kernel_stage):
 
 
 # ------------------------------------------------------------------ oracle timing ---------
-def oracle_sample(wl, cpu_inp, quotas_np, target_s=15.0):
-    """Time the fp64 oracle on a leading slice of the tokens; returns (pairs/s, info)."""
-    import oracle
-    T = wl.T
-    ts = min(T, 512)
-    while True:
-        sub = {n: (v[:ts] if n not in ("w_gate_up", "w_down") else v) for n, v in cpu_inp.items()}
-        loads, q = oracle.plan_quotas(sub["topk_idx"].numpy(), wl.E, *W.quota_policy(wl)[:4],
-                                      explicit=W.quota_policy(wl)[4])
+def oracle_inputs(inp):
+    """The workload's tensors as numpy arrays for the oracle, floating point widened to fp64 where
+    the tensors live (the widening is input preparation, not the oracle's work)."""
+    return {n: (v.double() if v.dtype.is_floating_point else v).cpu().numpy()
+            for n, v in inp.items() if n != "logits"}
+
+
+class OracleSample:
+    """The fp64 oracle on a bounded sample of a workload: every token and every pair is scored and
+    selected, and the backward runs on the retained rows of a subset S of the experts (the other
+    experts' quotas are set to 0, so the oracle computes nothing for them).  An expert's backward
+    depends on its own rows only, so a kept row costs the oracle what it costs in the whole
+    workload.  S takes experts in proportion to the retained rows they hold (see __init__) until
+    one call takes about the target time."""
+
+    def __init__(self, wl, npi):
+        import oracle
+        self.oracle, self.wl, self.npi = oracle, wl, npi
+        kind, num, den, cap, expl = W.quota_policy(wl)
+        self.loads, self.quotas = oracle.plan_quotas(npi["topk_idx"], wl.E, kind, num, den, cap, expl)
+        kept = np.minimum(np.maximum(self.quotas, 0), self.loads)
+        # experts in the order of the retained rows they hold: the i-th pick is the expert that
+        # holds the row at quantile vdc(i) (van der Corput: 1/2, 1/4, 3/4, 1/8, ...) of all retained
+        # rows, so a sample of any size weighs experts by their share of the work
+        ends = np.cumsum(kept)
+        total = int(ends[-1]) if len(ends) else 0
+        order, seen, i = [], set(), 1
+        while total > 0 and len(seen) < int(np.count_nonzero(kept)) and i < 64 * wl.E:
+            v, f, n = 0.0, 0.5, i
+            while n:
+                v += f * (n & 1)
+                n >>= 1
+                f *= 0.5
+            e = int(np.searchsorted(ends, v * total, side="right"))
+            if e < wl.E and kept[e] > 0 and e not in seen:
+                seen.add(e)
+                order.append(e)
+            i += 1
+        order += [e for e in range(wl.E) if e not in seen and kept[e] > 0]
+        order += [e for e in range(wl.E) if kept[e] == 0]
+        self.order = order
+        self.cum_rows = np.concatenate([[0], np.cumsum(kept[self.order])])
+        self.n = wl.E
+
+    def quotas_for(self, n):
+        q = np.zeros_like(self.quotas)
+        sel = self.order[:n]
+        q[sel] = self.quotas[sel]
+        return q
+
+    def run(self, n=None):
+        n = self.n if n is None else n
         t0 = time.perf_counter()
-        out = oracle.pruned_backward(sub, q)
-        dt = time.perf_counter() - t0
-        R = int(out["seg_offsets"][-1])
-        if dt >= target_s / 4 or ts >= T:
-            return R / dt, {"tokens": ts, "retained": R, "seconds": dt}
-        ts = min(T, int(ts * max(2.0, min(8.0, target_s / 2 / max(dt, 1e-3)))))
+        out = self.oracle.pruned_backward(self.npi, self.quotas_for(n))
+        return int(out["seg_offsets"][-1]), time.perf_counter() - t0
+
+    def calibrate(self, target_s, rounds=4):
+        """Pick |S| so that one call takes about target_s.  The fixed cost comes from a call with no
+        expert; the per-row cost from the latest measured call, refined over a few calls (the cost
+        of a row depends on its expert's size)."""
+        _, f = self.run(0)
+        n = 1
+        r, t = self.run(n)
+        for _ in range(rounds):
+            c = max(t - f, 1e-6) / max(r, 1)
+            m = 1
+            while m < self.wl.E and f + c * self.cum_rows[m + 1] <= target_s:
+                m += 1
+            if m == n:
+                break
+            n = m
+            r, t = self.run(n)
+            if t > 1.5 * target_s and n > 1:
+                n = max(1, n // 2)
+                r, t = self.run(n)
+        self.n = n
+        return n
+
+    def describe(self):
+        return (f"fp64 numpy oracle: score and selection of all {self.wl.P} pairs, backward of the "
+                f"{int(self.cum_rows[self.n])} retained rows of {self.n} of {self.wl.E} experts")
+
+
+def oracle_baseline(wl, inp, target_s=12.0, single_target_s=6.0):
+    """cpu_baseline of the bench line: the oracle on the host cores (all threads of its BLAS pool),
+    then the same on one thread, each on a sample sized to about its target time."""
+    from threadpoolctl import threadpool_limits
+    smp = OracleSample(wl, oracle_inputs(inp))
+    smp.calibrate(target_s)
+    R, dt = smp.run()
+    out = {"value": round(R / dt, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
+           "sample": f"{smp.describe()} ({dt:.1f} s)"}
+    with threadpool_limits(1):
+        smp1 = OracleSample(wl, smp.npi)
+        smp1.calibrate(single_target_s)
+        R1, dt1 = smp1.run()
+    out["single_thread"] = {"value": round(R1 / dt1, 1), "unit": UNIT, "cores": 1,
+                            "sample": f"{smp1.describe()} ({dt1:.1f} s)"}
+    return out
 
 
 def cpu_threads():
@@ -204,7 +291,7 @@ def main():
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--workload", default="qwen3_t8k_d20", choices=sorted(W.WORKLOADS))
+    ap.add_argument("--workload", default="glm45_t32k_d20", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05 (comparison only)")
     ap.add_argument("--no-extras", action="store_true",
@@ -253,7 +340,7 @@ def main():
         if evs is not None:
             evs[2].record(stream)
         lrm.lrm_compact(pb.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], pb.cap,
-                        dy_c=pb.dy_c, x_c=pb.x_c, h_c=pb.h_c, phi_c=pb.phi_c)
+                        dy_c=pb.dy_c, x_c=pb.x_c, h_c=pb.h_c, phi_c=pb.phi_c, dev_status=pb.dev_status)
         if evs is not None:
             evs[3].record(stream)
         lrm.lrm_grouped_backward(pb.seg_offsets, pb.dy_c, pb.x_c, pb.h_c, pb.phi_c, inp["w_gate_up"],
@@ -261,7 +348,7 @@ def main():
                                  dh_c=pb.dh_c, dx_c=pb.dx_c, ws=pb.ws, flags=flags, dev_status=pb.dev_status)
         if evs is not None:
             evs[4].record(stream)
-        lrm.lrm_scatter_dx(pb.row_of_pair, pb.dx_c, wl.T, wl.k, dx=pb.dx)
+        lrm.lrm_scatter_dx(pb.row_of_pair, pb.dx_c, wl.T, wl.k, dx=pb.dx, cap=pb.cap, dev_status=pb.dev_status)
         if evs is not None:
             evs[5].record(stream)
 
@@ -325,7 +412,7 @@ def main():
                       "frac_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4)})
         stage_info[s] = d
     dom = max(stages, key=lambda s: stage_ms[s])
-    tr = recorded_traffic(dom)
+    tr = recorded_traffic(dom, wl.name)
     # the binding roofline of the dominant stage is the one whose ideal time is longer
     t_hbm = alg[dom]["bytes"] / (pk["hbm_gbs"] * 1e9)
     t_tc = alg[dom].get("flops", 0) / (pk["bf16_tflops_sustained"] * 1e12) if wl.dtype == "bf16" else 0.0
@@ -364,12 +451,7 @@ def main():
         "next_rows": nxt,
     }
     if not args.no_cpu_baseline and world == 1:
-        cpu_inp = {n: v.cpu() for n, v in inp.items()}
-        v, info = oracle_sample(wl, cpu_inp, None)
-        out["cpu_baseline"] = {"value": round(v, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                               "sample": f"fp64 numpy oracle, whole path on the first {info['tokens']} of "
-                                         f"{wl.T} tokens ({info['retained']} retained pairs, "
-                                         f"{info['seconds']:.1f} s)"}
+        out["cpu_baseline"] = oracle_baseline(wl, inp)
     print(json.dumps(out), flush=True)
     if pg:
         pg.destroy_process_group()
@@ -437,6 +519,21 @@ def next_rows(args, wl, inp, quotas, flags, dev, stream, ms_step, pk):
                               "vs_materialised": round(ms_step / ms_g, 4), "steps": n,
                               "dev_status": int(pb.dev_status.item())}
     del pb
+    # recompute variant: the forward kept x and ||phi_u||^2 only; the retained rows' h and phi are
+    # recomputed from x (one more var-M GEMM) instead of being compacted from saved state
+    _, phi_sq = lrm.lrm_swiglu_forward(inp["h"])
+    lean = {nm: v for nm, v in inp.items() if nm not in ("h", "phi")}
+    lean["phi_sq"] = phi_sq
+    pb = lrm.PrunedBackward(wl.T, wl.k, wl.E, wl.H, wl.I, dtype=wl.torch_dtype, device=dev, flags=flags,
+                            compaction="recompute")
+    ms_r = _event_ms(lambda: pb.run(lean, quotas), n, stream)
+    b_el = 2 if wl.dtype == "bf16" else 4
+    out["recompute"] = {"ms_per_step": round(ms_r, 4), "value": round(R / (ms_r / 1e3), 1), "unit": UNIT,
+                        "vs_materialised": round(ms_step / ms_r, 4), "steps": n,
+                        "extra_flops": 4 * wl.H * wl.I * R,
+                        "forward_state_not_kept_bytes": wl.P * 3 * wl.I * b_el - 4 * wl.P,
+                        "dev_status": int(pb.dev_status.item())}
+    del pb, lean, phi_sq
     scores = torch.empty(wl.P, dtype=torch.float32, device=dev)
 
     def hbm(ms, by):
@@ -507,27 +604,28 @@ def end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev):
     return {"value": round(pairs_per_second(R_total, steps, ms), 1), "unit": UNIT, "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps, "ms_per_step": round(ms / steps, 4),
             "path": "HostPipeline: pinned host inputs, H2D on a copy stream overlapping the previous step, "
-                    "dX + seg_offsets read back every step"}
+                    "dX + seg_offsets read back every step; the fp32 weight gradients stay on the device "
+                    "(the optimizer step that consumes them runs there)"}
 
 
 def reference_arm(args, wl, rank, world):
-    """fp64 CPU oracle on the host cores: each step is a bounded sample of the workload."""
+    """fp64 CPU oracle on the host cores: each step is one oracle call on a bounded sample of the
+    workload (OracleSample; the sample is sized during the warm-up steps to about 4 s per call)."""
     if rank != 0:
         return
-    import oracle
-    # inputs drawn on the CPU with the same generator (the oracle never touches the GPU)
-    ts = min(wl.T, 1024 if wl.H * wl.I <= 2048 * 768 else 512)
-    sub_wl = wl if ts == wl.T else W.Workload(wl.name + "_sample", ts, wl.H, wl.I, wl.E, wl.k, wl.dtype,
-                                              wl.zipf_s, wl.g_std, wl.quota)
-    inp = W.generate(sub_wl, "cpu", seed=0)
-    kind, num, den, cap, expl = W.quota_policy(wl)
-    _, q = oracle.plan_quotas(inp["topk_idx"].numpy(), wl.E, kind, num, den, cap, expl)
-    for _ in range(args.warmup):
-        oracle.pruned_backward(inp, q)
+    # inputs drawn with the same generator, on the GPU where there is one (drawing the largest
+    # workloads on the host takes minutes); the oracle itself runs on the host only
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp = W.generate(wl, dev, seed=0)
+    smp = OracleSample(wl, oracle_inputs(inp))
+    del inp
+    smp.calibrate(4.0)
+    for _ in range(max(0, args.warmup - 2)):
+        smp.run()
     t0 = time.perf_counter()
     R = 0
     for _ in range(args.steps):
-        R = int(oracle.pruned_backward(inp, q)["seg_offsets"][-1])
+        R, _ = smp.run()
     dt = time.perf_counter() - t0
     value = R * args.steps / dt
     print(json.dumps({
@@ -535,10 +633,9 @@ def reference_arm(args, wl, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "quota": quota_text(wl), "sample_tokens": ts},
+                   "quota": quota_text(wl), "sample_experts": smp.n, "sample_rows": int(smp.cum_rows[smp.n])},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
-                         "sample": f"fp64 numpy oracle, whole path on {ts} of {wl.T} tokens per step "
-                                   f"({R} retained pairs)"},
+                         "sample": smp.describe()},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }), flush=True)
 

@@ -30,8 +30,16 @@
  *    Device-detected errors are written to the optional `dev_status` word (int32, device
  *    memory, caller zeroes it): the first error code wins (atomic compare-and-swap from 0).
  *    The caller reads it whenever it chooses; the library never does.
- *  - Limits: 1 <= E <= LRM_MAX_EXPERTS, 1 <= k <= LRM_MAX_TOPK, P <= INT32_MAX,
- *    H and I positive multiples of 8.
+ *  - Limits: 1 <= E <= LRM_MAX_EXPERTS, 1 <= k <= LRM_MAX_TOPK, P <= INT32_MAX (checked
+ *    without forming an overflowing product), H and I positive multiples of 8.
+ *  - Index arrays handed from one call to the next (row_of_pair, seg_offsets) are checked
+ *    where they are used: an index outside its range is never followed; the pair (or the
+ *    whole grouped backward) is skipped and the status word records why.  A build with
+ *    -DLRM_DEBUG (liblrm_debug.so) adds the same kind of check to every index the kernels
+ *    form themselves (bucket slots, compacted rows of a tile, gathered pair rows); a failed
+ *    check records LRM_ERR_BAD_INDEX and skips the access, it never traps.
+ *  - Each entry point opens an NVTX range of its own name around its host work when the
+ *    environment variable LRM_NVTX is 1 at the library's first call (off otherwise).
  *  - The kernels of lrm_score, lrm_select, lrm_select_static, lrm_compact,
  *    lrm_grouped_backward (tensor-core path) and lrm_scatter_dx use programmatic dependent launch: each waits (griddepcontrol.wait) for the
  *    work queued before it on the stream to complete before it touches memory, and lets the
@@ -64,8 +72,11 @@ typedef enum lrm_status {
   LRM_ERR_CAPACITY = 6,    /* device: sum of kept rows exceeds `cap` (nothing is kept)  */
   LRM_ERR_NONFINITE = 7,   /* device: a score is NaN or infinite                        */
   LRM_ERR_TIMEOUT = 8,     /* device: a bounded wait gave up                            */
-  LRM_ERR_BAD_INDEX = 9,   /* device: an expert id outside [0, E) (pair treated as dropped) */
-  LRM_ERR_UNSUPPORTED = 10 /* no kernel for this device / configuration                 */
+  LRM_ERR_BAD_INDEX = 9,   /* device: an expert id outside [0, E), or a compacted row
+                              outside [-1, cap) (the pair is treated as dropped)        */
+  LRM_ERR_UNSUPPORTED = 10, /* no kernel for this device / configuration                */
+  LRM_ERR_BAD_SEGMENTS = 11 /* device: seg_offsets[0] != 0, a decreasing step, or
+                              seg_offsets[E] > cap (the grouped backward computes nothing) */
 } lrm_status;
 
 typedef enum lrm_dtype { LRM_BF16 = 0, LRM_F32 = 1 } lrm_dtype;
@@ -164,15 +175,18 @@ lrm_status lrm_select(const int32_t* topk_idx, const float* scores, const int32_
  *   x_c[r] = x_t,   h_c[r] = h_u,   phi_c[r] = phi_u
  *   row_of_pair [T*k] int32 (from lrm_select), alpha [T*k] fp32, g [T,H], x [T,H],
  *   h [T*k, 2I], phi [T*k, I]  ->  dy_c [cap,H], x_c [cap,H], h_c [cap,2I], phi_c [cap,I] (dt).
- * Rows are visited token by token, so g_t and x_t are read once per token.  Rows >= cap are
- * skipped.  With x_c, h_c and phi_c all NULL only dy_c is written (x, h, phi may then be NULL):
- * the compaction-free variant, whose grouped backward reads those rows in place
- * (lrm_grouped_backward_gather).
+ * Rows are visited token by token, so g_t and x_t are read once per token.  A row_of_pair
+ * entry outside [-1, cap) is not followed: the pair is skipped and LRM_ERR_BAD_INDEX is set in
+ * dev_status.  With x_c, h_c and phi_c all NULL only dy_c is written (x, h, phi may then be
+ * NULL): the compaction-free variant, whose grouped backward reads those rows in place
+ * (lrm_grouped_backward_gather).  With h_c and phi_c NULL and x_c given, dy_c and x_c are
+ * written (h and phi may be NULL): the variant whose forward did not keep h and phi, which
+ * lrm_recompute_forward then rebuilds for the retained rows.
  */
 lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x,
                        const void* h, const void* phi, int64_t T, int32_t k, int32_t H, int32_t I,
                        lrm_dtype dt, int64_t cap, void* dy_c, void* x_c, void* h_c, void* phi_c,
-                       cudaStream_t stream);
+                       int32_t* dev_status, cudaStream_t stream);
 
 /*
  * SwiGLU expert backward as variable-size grouped GEMMs driven by the retained row counts
@@ -185,7 +199,9 @@ lrm_status lrm_compact(const int32_t* row_of_pair, const float* alpha, const voi
  *   dx_c[e]       = dh_c[e] w_gate_up[e]                             [cap,H]  dt
  * An expert with R_e = 0 gets dw = 0 exactly.  w_gate_up [E,2I,H] (gate rows first),
  * w_down [E,H,I].  Accumulation is fp32.  `flags` is LRM_GEMM_DEFAULT or LRM_GEMM_FORCE_SIMT.
- * seg_offsets must be non-decreasing with seg_offsets[E] <= cap (as lrm_select writes them).
+ * seg_offsets must start at 0, be non-decreasing and end at seg_offsets[E] <= cap (as lrm_select
+ * writes them).  The kernels check this on the device before any tile runs: otherwise they set
+ * LRM_ERR_BAD_SEGMENTS in dev_status and compute nothing (every output keeps its old contents).
  * Optional row_dot [cap] fp32 (NULL skips it; 4-byte aligned): for every retained row
  * r < seg_offsets[E], row_dot[r] = sum_i dphi[r,i] * phi~[r,i], where phi~ = SiLU(gate)*up is
  * recomputed in fp32 from h_c inside the same epilogue; for the pair u = (t, e) of row r that is
@@ -212,14 +228,32 @@ lrm_status lrm_grouped_backward(const int32_t* seg_offsets, const void* dy_c, co
  * operand tiles; the SwiGLU epilogue reads h by index.  Results are bit-identical to
  * lrm_grouped_backward on the materialised buffers (same values, same order of arithmetic).
  *   kept_pair [cap] int32, x [T,H], h [T*k,2I], phi [T*k,I] (dt); the rest as in
- *   lrm_grouped_backward.  Errors as there.
+ *   lrm_grouped_backward.  Errors as there; a kept_pair entry outside [0, T*k) is not followed
+ *   (its row reads as zeros) and sets LRM_ERR_BAD_INDEX in dev_status.
  */
-lrm_status lrm_grouped_backward_gather(const int32_t* seg_offsets, const int32_t* kept_pair, int32_t k,
+lrm_status lrm_grouped_backward_gather(const int32_t* seg_offsets, const int32_t* kept_pair, int64_t T, int32_t k,
                                        const void* dy_c, const void* x, const void* h, const void* phi,
                                        const void* w_gate_up, const void* w_down, int32_t E, int32_t H, int32_t I,
                                        lrm_dtype dt, int64_t cap, float* dw_gate_up, float* dw_down, void* dh_c,
                                        void* dx_c, float* row_dot, void* ws, size_t ws_bytes, int32_t flags,
                                        int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * The saved forward state of the retained rows, recomputed from their x rows (the variant of
+ * "The part that is easy to get wrong" whose forward keeps x and the score's ||phi_u||^2 instead of
+ * h and phi; lrm_swiglu_forward emits the norms).  For each expert e over its segment (R_e rows,
+ * read on the device from seg_offsets):
+ *   h_c[r]   = round_dt(W_gate_up[e] x_c[r])                     [cap,2I] dt (gate first), fp32 sums
+ *   phi_c[r] = round_dt(SiLU(gate) * up), gate / up taken from the stored h_c[r]   [cap,I] dt
+ * i.e. what the forward's expert projection and lrm_swiglu_forward would have stored for those
+ * pairs.  x_c [cap,H], w_gate_up [E,2I,H].  Rows >= seg_offsets[E] are not written.  ws: scratch of
+ * at least lrm_workspace_size bytes (shared with the other calls on the stream).  The same
+ * segment check as lrm_grouped_backward (LRM_ERR_BAD_SEGMENTS: nothing computed).  flags as
+ * there (fp32 inputs, or LRM_GEMM_FORCE_SIMT, run on the CUDA cores).
+ */
+lrm_status lrm_recompute_forward(const int32_t* seg_offsets, const void* x_c, const void* w_gate_up, int32_t E,
+                                 int32_t H, int32_t I, lrm_dtype dt, int64_t cap, void* h_c, void* phi_c, void* ws,
+                                 size_t ws_bytes, int32_t flags, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * Routing-weight gradient of the pairs.  The layer output is out_t = sum_j alpha_{t,j} y_{t,j}
@@ -243,9 +277,11 @@ lrm_status lrm_router_grad(const int32_t* row_of_pair, const float* alpha, const
  * pairs, summed in fp32 and rounded once to dt; a token with no kept pair gets 0.  No atomics:
  * the result is deterministic.
  *   row_of_pair [T*k] int32, dx_c [cap,H] dt  ->  dx [T,H] dt.
+ * cap is the row count of dx_c: an entry of row_of_pair outside [-1, cap) is not followed (the
+ * pair adds nothing) and sets LRM_ERR_BAD_INDEX in the optional dev_status.
  */
 lrm_status lrm_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H,
-                          lrm_dtype dt, void* dx, cudaStream_t stream);
+                          lrm_dtype dt, int64_t cap, void* dx, int32_t* dev_status, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------------
  * Forward-side steps beside the path, each fused with the work next to it.
@@ -313,7 +349,9 @@ lrm_status lrm_selftest_wait_timeout(int32_t* dev_status, int64_t limit_ns, cuda
  *     return LRM_ERR_SHAPE before any GPU work — use lrm_select with a workspace for them.
  *   - The first call on a device, with that device current, looks up the array's device address
  *     (cudaGetSymbolAddress) and remembers it; make that first call before any stream capture.
- *     A failed look-up returns LRM_ERR_CUDA.
+ *     The address is kept together with the identity of the CUDA context it belongs to: after a
+ *     cudaDeviceReset (a new primary context) the next call looks it up again, so that call too
+ *     should come before any stream capture.  A failed look-up returns LRM_ERR_CUDA.
  *   - All calls share the one array and leave their data in it.  Nothing in it needs to start
  *     at zero, but calls that overlap on the GPU (different streams, or threads without ordering
  *     between their streams) race on it: serialise them.

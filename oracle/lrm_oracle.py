@@ -24,7 +24,7 @@ H hidden, I expert intermediate. h_u = [gate_u; up_u] (2I), phi_u = SiLU(gate_u)
 W_gate_up[e] (2I x H, gate rows first), W_down[e] (H x I), upstream gradient g_t (H) of the
 layer output out_t = sum_j alpha_{t,j} W_down[e_{t,j}] phi_{t,j}.
 
-Readings where the pages are silent (each also listed in the design doc):
+Readings where the pages are silent:
   * phi is the input of the down projection, so G_u = (alpha_u g_t) phi_u^T is exactly
     pair u's term of dW_down ("protected expert projection", [EN] "LRM: ...").
   * A dropped pair contributes nothing to any part of the expert backward (dW_down,
@@ -335,6 +335,54 @@ def pruned_backward(inp, quotas, scores=None):
     seg, kept, rop = select(idx, sel_scores, quotas, E)
     dY_c, X_c, H_c, Phi_c = compact(kept, _np(inp["alpha"]), _np(inp["g"]), _np(inp["x"]),
                                     _np(inp["h"]), _np(inp["phi"]), k)
+    dWgu, dWd, dH_c, dX_c = expert_backward(seg, dY_c, X_c, H_c, Phi_c,
+                                            _np(inp["w_gate_up"]), _np(inp["w_down"]))
+    dX = scatter_dx(rop, dX_c, T, k)
+    return {"scores": R_u, "seg_offsets": seg, "kept_pair": kept, "row_of_pair": rop,
+            "dY_c": dY_c, "X_c": X_c, "H_c": H_c, "Phi_c": Phi_c,
+            "dH_c": dH_c, "dX_c": dX_c, "dw_gate_up": dWgu, "dw_down": dWd, "dx": dX}
+
+
+# ----------------------------------------------------------------------------------------
+# saved state recomputed from x  ([EN] "The part that is easy to get wrong": the pages insist on
+# physically compacted rows; a variant that keeps less forward state recomputes, for the retained
+# rows only, what the forward would have saved.  Reading: the forward keeps x and the score's
+# ||phi_u||^2 (see swiglu_forward), and the backward forms h_u = W_gate_up[e] x_t and
+# phi_u = SiLU(gate_u) * up_u again for the pairs it keeps.)
+# ----------------------------------------------------------------------------------------
+def recompute_saved_state(kept_pair, topk_idx, x, w_gate_up, k):
+    """For the kept pairs u = kept_pair[r] (token t = u // k, expert e = topk_idx[u]):
+      H_c[r] = W_gate_up[e] x_t  (2I: gate rows first),  Phi_c[r] = SiLU(gate) * up  (swiglu_forward),
+    in fp64.  Pinned: the pruned backward on this recomputed state equals torch fp64 autograd of
+    the explicit forward at quota = load; a gate/up swap fails that pin."""
+    kp = np.asarray(kept_pair, dtype=np.int64)
+    idx = np.asarray(topk_idx).reshape(-1).astype(np.int64)
+    X = np.asarray(x)
+    Wgu = np.asarray(w_gate_up)
+    I = Wgu.shape[1] // 2
+    H_c = np.zeros((kp.shape[0], 2 * I))
+    for r, u in enumerate(kp):
+        H_c[r] = Wgu[idx[u]].astype(np.float64) @ X[u // k].astype(np.float64)
+    Phi_c, _ = swiglu_forward(H_c, I)
+    return H_c, Phi_c
+
+
+def pruned_backward_recompute(inp, quotas, scores=None):
+    """The pruned backward of a forward that kept x and phi_sq = ||phi_u||^2 instead of h and phi:
+    score from the norms, select, compact dY_c and X_c, recompute H_c and Phi_c for the kept rows,
+    then the grouped backward and the return to token order.  inp holds topk_idx, alpha, x, g,
+    phi_sq [T,k], w_gate_up, w_down.  `scores` overrides the selection scores as in pruned_backward."""
+    idx = _np(inp["topk_idx"])
+    T, k = idx.shape
+    E = _np(inp["w_down"]).shape[0]
+    R_u = lrm_scores_from_norms(_np(inp["alpha"]), _np(inp["g"]), _np(inp["phi_sq"]))
+    sel_scores = R_u if scores is None else _np(scores)
+    seg, kept, rop = select(idx, sel_scores, quotas, E)
+    a = np.asarray(_np(inp["alpha"])).reshape(-1)[kept].astype(np.float64)
+    t = kept // k
+    dY_c = a[:, None] * np.asarray(_np(inp["g"]))[t].astype(np.float64)
+    X_c = np.asarray(_np(inp["x"]))[t].astype(np.float64)
+    H_c, Phi_c = recompute_saved_state(kept, idx, _np(inp["x"]), _np(inp["w_gate_up"]), k)
     dWgu, dWd, dH_c, dX_c = expert_backward(seg, dY_c, X_c, H_c, Phi_c,
                                             _np(inp["w_gate_up"]), _np(inp["w_down"]))
     dX = scatter_dx(rop, dX_c, T, k)

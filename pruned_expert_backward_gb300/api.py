@@ -165,10 +165,16 @@ def lrm_select(topk_idx, scores, quotas, E, cap=None, seg_offsets=None, kept_pai
     return seg_offsets, kept_pair, row_of_pair
 
 
-def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=None, phi_c=None, dy_only=False):
-    """dy_only: write only dy_c (the compaction-free variant; x_c, h_c, phi_c are returned as None)."""
+def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=None, phi_c=None, dy_only=False,
+                dev_status=None, x_only=False, k=None, I=None):
+    """dy_only: write only dy_c (the compaction-free variant; x_c, h_c, phi_c are returned as None).
+    x_only: write dy_c and x_c (h and phi may be None: the variant that recomputes them; k and I
+    must then be given)."""
     T, H = g.shape
-    k, I = phi.shape[-2], phi.shape[-1]
+    if phi is not None:
+        k, I = phi.shape[-2], phi.shape[-1]
+    elif k is None or I is None:
+        raise ValueError("k and I are needed when phi is not given")
     dev, dt = g.device, g.dtype
     rows = max(int(cap), 1)
     dy_c = torch.empty(rows, H, dtype=dt, device=dev) if dy_c is None else dy_c
@@ -176,12 +182,16 @@ def lrm_compact(row_of_pair, alpha, g, x, h, phi, cap, dy_c=None, x_c=None, h_c=
         x_c = h_c = phi_c = None
     else:
         x_c = torch.empty(rows, H, dtype=dt, device=dev) if x_c is None else x_c
-        h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
-        phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
+        if x_only:
+            h_c = phi_c = None
+        else:
+            h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
+            phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
     _ok(L.load().lrm_compact(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(alpha, "alpha", torch.float32),
-                             _cuda(g, "g"), _cuda(x, "x", dt), _cuda(h, "h", dt), _cuda(phi, "phi", dt), T, k, H, I,
+                             _cuda(g, "g"), _opt(x, "x", dt), _opt(h, "h", dt), _opt(phi, "phi", dt), T, k, H, I,
                              _dt(g), int(cap), _cuda(dy_c, "dy_c", dt), _opt(x_c, "x_c", dt),
-                             _opt(h_c, "h_c", dt), _opt(phi_c, "phi_c", dt), _stream()), "lrm_compact")
+                             _opt(h_c, "h_c", dt), _opt(phi_c, "phi_c", dt),
+                             _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_compact")
     return dy_c, x_c, h_c, phi_c
 
 
@@ -225,7 +235,7 @@ def lrm_grouped_backward_gather(seg_offsets, kept_pair, k, dy_c, x, h, phi, w_ga
         ws_rows = int(cap) if row_dot is not None else 0
         ws = torch.empty(lrm_workspace_size(ws_rows, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
     _ok(L.load().lrm_grouped_backward_gather(
-        _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(kept_pair, "kept_pair", torch.int32), int(k),
+        _cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(kept_pair, "kept_pair", torch.int32), x.shape[0], int(k),
         _cuda(dy_c, "dy_c", dt), _cuda(x, "x", dt), _cuda(h, "h", dt), _cuda(phi, "phi", dt),
         _cuda(w_gate_up, "w_gate_up", dt), _cuda(w_down, "w_down", dt), E, H, I, _dt(w_down), int(cap),
         _cuda(dw_gate_up, "dw_gate_up", torch.float32), _cuda(dw_down, "dw_down", torch.float32),
@@ -233,6 +243,26 @@ def lrm_grouped_backward_gather(seg_offsets, kept_pair, k, dy_c, x, h, phi, w_ga
         _cuda(ws, "ws"), ws.numel(), int(flags), _opt(dev_status, "dev_status", torch.int32), _stream()),
         "lrm_grouped_backward_gather")
     return dw_gate_up, dw_down, dh_c, dx_c
+
+
+def lrm_recompute_forward(seg_offsets, x_c, w_gate_up, cap, h_c=None, phi_c=None, ws=None, flags=L.LRM_GEMM_DEFAULT,
+                          dev_status=None):
+    """h_c = W_gate_up[e] x_c and phi_c = SiLU(gate) * up for the retained rows (the saved forward
+    state recomputed from x).  Returns (h_c [cap,2I], phi_c [cap,I])."""
+    E, I2, H = w_gate_up.shape
+    I = I2 // 2
+    dev, dt = w_gate_up.device, w_gate_up.dtype
+    rows = max(int(cap), 1)
+    h_c = torch.empty(rows, 2 * I, dtype=dt, device=dev) if h_c is None else h_c
+    phi_c = torch.empty(rows, I, dtype=dt, device=dev) if phi_c is None else phi_c
+    if ws is None:
+        ws = torch.empty(lrm_workspace_size(0, 1, E, H, I, dt), dtype=torch.uint8, device=dev)
+    _ok(L.load().lrm_recompute_forward(_cuda(seg_offsets, "seg_offsets", torch.int32), _cuda(x_c, "x_c", dt),
+                                       _cuda(w_gate_up, "w_gate_up", dt), E, H, I, _dt(w_gate_up), int(cap),
+                                       _cuda(h_c, "h_c", dt), _cuda(phi_c, "phi_c", dt), _cuda(ws, "ws"), ws.numel(),
+                                       int(flags), _opt(dev_status, "dev_status", torch.int32), _stream()),
+        "lrm_recompute_forward")
+    return h_c, phi_c
 
 
 def lrm_router_grad(row_of_pair, alpha, row_dot, T, k, cap, dalpha=None):
@@ -244,11 +274,16 @@ def lrm_router_grad(row_of_pair, alpha, row_dot, T, k, cap, dalpha=None):
     return dalpha
 
 
-def lrm_scatter_dx(row_of_pair, dx_c, T, k, dx=None):
+def lrm_scatter_dx(row_of_pair, dx_c, T, k, dx=None, cap=None, dev_status=None):
+    """cap: rows of dx_c that row_of_pair may name (default: all of dx_c's rows)."""
     H = dx_c.shape[1]
+    cap = dx_c.shape[0] if cap is None else int(cap)
+    if cap > dx_c.shape[0]:
+        raise ValueError(f"cap {cap} exceeds the {dx_c.shape[0]} rows of dx_c")
     dx = torch.empty(T, H, dtype=dx_c.dtype, device=dx_c.device) if dx is None else dx
     _ok(L.load().lrm_scatter_dx(_cuda(row_of_pair, "row_of_pair", torch.int32), _cuda(dx_c, "dx_c"), T, k, H,
-                                _dt(dx_c), _cuda(dx, "dx", dx_c.dtype), _stream()), "lrm_scatter_dx")
+                                _dt(dx_c), cap, _cuda(dx, "dx", dx_c.dtype),
+                                _opt(dev_status, "dev_status", torch.int32), _stream()), "lrm_scatter_dx")
     return dx
 
 
@@ -259,15 +294,19 @@ class PrunedBackward:
 
     cap defaults to T*k, which can never overflow; a caller that knows sum(min(quota, load))
     may pass it to shrink the compacted buffers.  router_grad=True also produces dL/dalpha of
-    every pair (`dalpha`, fp32 [T*k]; 0 for dropped pairs)."""
+    every pair (`dalpha`, fp32 [T*k]; 0 for dropped pairs).
+    compaction: "materialised" (the pages' physical compaction of dY, x, h, phi), "gather" (only dY
+    is compacted; x, h, phi rows are read in place) or "recompute" (the forward kept x and
+    ||phi_u||^2 only: dY and x are compacted and h, phi are recomputed for the retained rows)."""
 
     def __init__(self, T, k, E, H, I, dtype=torch.bfloat16, device="cuda", cap=None, flags=L.LRM_GEMM_DEFAULT,
                  router_grad=False, compaction="materialised"):
-        if compaction not in ("materialised", "gather"):
-            raise ValueError("compaction: 'materialised' (the pages' physical compaction) or 'gather'")
+        if compaction not in ("materialised", "gather", "recompute"):
+            raise ValueError("compaction: 'materialised' (the pages' physical compaction), 'gather' or 'recompute'")
         self.T, self.k, self.E, self.H, self.I = T, k, E, H, I
         self.dtype, self.flags, self.router_grad = dtype, flags, router_grad
         self.gather = compaction == "gather"
+        self.recompute = compaction == "recompute"
         self.cap = T * k if cap is None else int(cap)
         dev = torch.device(device)
         rows = max(self.cap, 1)
@@ -294,7 +333,10 @@ class PrunedBackward:
     def run(self, inp, quotas):
         """inp: dict with topk_idx [T,k] int32, alpha [T,k] fp32, x, g [T,H], h [T,k,2I], phi [T,k,I],
         w_gate_up [E,2I,H], w_down [E,H,I] (CUDA), and optionally phi_sq fp32 [T,k] (||phi_u||^2 from
-        lrm_swiglu_forward; the score then reads it instead of phi).  quotas: int32 [E] (CUDA)."""
+        lrm_swiglu_forward; the score then reads it instead of phi).  quotas: int32 [E] (CUDA).
+        compaction="recompute" needs phi_sq and neither h nor phi."""
+        if self.recompute:
+            return self._run_recompute(inp, quotas)
         if inp.get("phi_sq") is not None:  # the forward handed over ||phi_u||^2
             lrm_score_norms(inp["alpha"], inp["g"], inp["phi_sq"], scores=self.scores, dev_status=self.dev_status)
         else:
@@ -302,7 +344,8 @@ class PrunedBackward:
         lrm_select(inp["topk_idx"], self.scores, quotas, self.E, cap=self.cap, seg_offsets=self.seg_offsets,
                    kept_pair=self.kept_pair, row_of_pair=self.row_of_pair, ws=self.ws, dev_status=self.dev_status)
         lrm_compact(self.row_of_pair, inp["alpha"], inp["g"], inp["x"], inp["h"], inp["phi"], self.cap,
-                    dy_c=self.dy_c, x_c=self.x_c, h_c=self.h_c, phi_c=self.phi_c, dy_only=self.gather)
+                    dy_c=self.dy_c, x_c=self.x_c, h_c=self.h_c, phi_c=self.phi_c, dy_only=self.gather,
+                    dev_status=self.dev_status)
         if self.gather:
             lrm_grouped_backward_gather(self.seg_offsets, self.kept_pair, self.k, self.dy_c, inp["x"], inp["h"],
                                         inp["phi"], inp["w_gate_up"], inp["w_down"], self.cap,
@@ -314,7 +357,29 @@ class PrunedBackward:
                                  inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
                                  dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
                                  dev_status=self.dev_status, row_dot=self.row_dot)
-        lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx)
+        lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx, cap=self.cap,
+                       dev_status=self.dev_status)
+        if self.router_grad:
+            lrm_router_grad(self.row_of_pair, inp["alpha"], self.row_dot, self.T, self.k, self.cap,
+                            dalpha=self.dalpha)
+        return self
+
+    def _run_recompute(self, inp, quotas):
+        if inp.get("phi_sq") is None:
+            raise ValueError("compaction='recompute' scores from phi_sq (||phi_u||^2 of the forward)")
+        lrm_score_norms(inp["alpha"], inp["g"], inp["phi_sq"], scores=self.scores, dev_status=self.dev_status)
+        lrm_select(inp["topk_idx"], self.scores, quotas, self.E, cap=self.cap, seg_offsets=self.seg_offsets,
+                   kept_pair=self.kept_pair, row_of_pair=self.row_of_pair, ws=self.ws, dev_status=self.dev_status)
+        lrm_compact(self.row_of_pair, inp["alpha"], inp["g"], inp["x"], None, None, self.cap, dy_c=self.dy_c,
+                    x_c=self.x_c, x_only=True, k=self.k, I=self.I, dev_status=self.dev_status)
+        lrm_recompute_forward(self.seg_offsets, self.x_c, inp["w_gate_up"], self.cap, h_c=self.h_c, phi_c=self.phi_c,
+                              ws=self.ws, flags=self.flags, dev_status=self.dev_status)
+        lrm_grouped_backward(self.seg_offsets, self.dy_c, self.x_c, self.h_c, self.phi_c, inp["w_gate_up"],
+                             inp["w_down"], self.cap, dw_gate_up=self.dw_gate_up, dw_down=self.dw_down,
+                             dh_c=self.dh_c, dx_c=self.dx_c, ws=self.ws, flags=self.flags,
+                             dev_status=self.dev_status, row_dot=self.row_dot)
+        lrm_scatter_dx(self.row_of_pair, self.dx_c, self.T, self.k, dx=self.dx, cap=self.cap,
+                       dev_status=self.dev_status)
         if self.router_grad:
             lrm_router_grad(self.row_of_pair, inp["alpha"], self.row_dot, self.T, self.k, self.cap,
                             dalpha=self.dalpha)

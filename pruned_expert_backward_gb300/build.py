@@ -2,7 +2,11 @@
 
 Each .cu under csrc/ compiles to an object in parallel; the objects link into
 pruned_expert_backward_gb300/liblrm.so (static CUDA runtime, no other dependency).
-Run: python -m pruned_expert_backward_gb300.build   (or __graft_entry__.build()).
+The same sources compiled with -DLRM_DEBUG link into liblrm_debug.so: every index the
+kernels form themselves is checked as well (a failed check records LRM_ERR_BAD_INDEX in the
+status word and skips the access).  Both builds run side by side by default.
+Run: python -m pruned_expert_backward_gb300.build [--release-only] [-v]
+(or __graft_entry__.build()).
 """
 from __future__ import annotations
 
@@ -19,6 +23,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(PKG, "liblrm.so")
+LIB_DEBUG = os.path.join(PKG, "liblrm_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -38,8 +43,8 @@ def _newest_dep_mtime() -> float:
     return max(os.path.getmtime(p) for p in deps)
 
 
-def _compile(src: str, extra: list[str], verbose_ptxas: bool) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src).replace(".cu", ".o"))
+def _compile(src: str, extra: list[str], verbose_ptxas: bool, outdir: str = BUILD) -> str:
+    obj = os.path.join(outdir, os.path.basename(src).replace(".cu", ".o"))
     if os.path.exists(obj) and os.path.getmtime(obj) >= max(os.path.getmtime(src), _newest_dep_mtime()) \
             and not verbose_ptxas:
         return obj
@@ -52,21 +57,36 @@ def _compile(src: str, extra: list[str], verbose_ptxas: bool) -> str:
     return obj
 
 
-def build(verbose_ptxas: bool = False, extra: list[str] | None = None) -> str:
-    os.makedirs(BUILD, exist_ok=True)
-    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
-    with cf.ThreadPoolExecutor(max_workers=min(8, len(srcs))) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra or [], verbose_ptxas), srcs))
-    if os.path.exists(LIB) and os.path.getmtime(LIB) >= max(os.path.getmtime(o) for o in objs) and not extra:
-        return LIB
-    tmp = LIB + ".tmp"
+def _link(objs: list[str], lib: str, force: bool) -> str:
+    if os.path.exists(lib) and os.path.getmtime(lib) >= max(os.path.getmtime(o) for o in objs) and not force:
+        return lib
+    tmp = lib + ".tmp"
     cmd = [nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
+    os.replace(tmp, lib)
+    return lib
+
+
+def build(verbose_ptxas: bool = False, extra: list[str] | None = None, debug: bool = True) -> str:
+    """Compile and link liblrm.so (and, with debug, liblrm_debug.so); returns the release path."""
+    dbg_dir = os.path.join(BUILD, "debug")
+    os.makedirs(dbg_dir, exist_ok=True)
+    srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+    jobs = [(s, extra or [], BUILD) for s in srcs]
+    if debug:
+        jobs += [(s, (extra or []) + ["-DLRM_DEBUG"], dbg_dir) for s in srcs]
+    # the largest translation unit first, so it does not start last
+    jobs.sort(key=lambda j: -os.path.getsize(j[0]))
+    with cf.ThreadPoolExecutor(max_workers=min(16, os.cpu_count() or 8, len(jobs))) as ex:
+        objs = list(ex.map(lambda j: _compile(j[0], j[1], verbose_ptxas, j[2]), jobs))
+    rel = sorted(o for o in objs if os.path.dirname(o) == BUILD)
+    _link(rel, LIB, bool(extra))
+    if debug:
+        _link(sorted(o for o in objs if os.path.dirname(o) == dbg_dir), LIB_DEBUG, bool(extra))
     return LIB
 
 
 if __name__ == "__main__":
-    print(build(verbose_ptxas="-v" in sys.argv))
+    print(build(verbose_ptxas="-v" in sys.argv, debug="--release-only" not in sys.argv))

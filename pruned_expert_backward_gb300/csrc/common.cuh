@@ -16,6 +16,27 @@ __device__ __forceinline__ void set_status(int32_t* st, int32_t code) {
   if (st != nullptr) atomicCAS(st, 0, code);
 }
 
+// Index check of the LRM_DEBUG build: true when `cond` holds; otherwise records `code` in the
+// status word and yields false, so that the caller skips the access.  In the ordinary build it
+// is `true` and costs nothing.  Checks of indices that a caller hands in (row_of_pair,
+// seg_offsets, expert ids) are not made with it: those are always on.
+#ifdef LRM_DEBUG
+#define LRM_DCHECK(cond, st, code) ((cond) ? true : (::lrm::set_status((st), (code)), false))
+#else
+#define LRM_DCHECK(cond, st, code) true
+#endif
+
+// A compacted row index taken from row_of_pair: -1 (dropped) or a row in [0, cap).  Anything
+// else is recorded as LRM_ERR_BAD_INDEX and the pair is treated as dropped.
+__device__ __forceinline__ int64_t checked_row(int32_t r, int64_t cap, int32_t* st) {
+  if (r == -1) return -1;
+  if (r < 0 || (int64_t)r >= cap) {
+    set_status(st, LRM_ERR_BAD_INDEX);
+    return -1;
+  }
+  return r;
+}
+
 // 16-byte vector helpers.  A "vec" is 16 bytes: 8 bf16 or 4 fp32 elements.
 template <typename T> struct VecTraits;
 template <> struct VecTraits<__nv_bfloat16> { static constexpr int N = 8; };
@@ -132,7 +153,19 @@ inline cudaError_t launch_chained(void (*kernel)(KArgs...), dim3 grid, dim3 bloc
 
 }  // namespace lrm
 
-// Host-side launch helpers (defined in abi.cu).
+// NVTX range of an entry point (host side): pushed only when LRM_NVTX=1 at the first call.
 namespace lrm {
-lrm_status launch_check();
-}
+bool nvtx_enabled();
+void nvtx_push(const char* name);
+void nvtx_pop();
+struct NvtxRange {
+  bool on;
+  explicit NvtxRange(const char* name) : on(nvtx_enabled()) {
+    if (on) nvtx_push(name);
+  }
+  ~NvtxRange() {
+    if (on) nvtx_pop();
+  }
+};
+}  // namespace lrm
+#define LRM_NVTX_RANGE() ::lrm::NvtxRange lrm_nvtx_range_(__func__)

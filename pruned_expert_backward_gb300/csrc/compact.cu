@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
                                                       const T* __restrict__ x, const T* __restrict__ h,
                                                       const T* __restrict__ phi, int k, int H, int I, int64_t cap,
                                                       T* __restrict__ dy_c, T* __restrict__ x_c, T* __restrict__ h_c,
-                                                      T* __restrict__ phi_c) {
+                                                      T* __restrict__ phi_c, int32_t* __restrict__ status) {
   chain_wait();
   constexpr int VN = VecTraits<T>::N;
   __shared__ int64_t s_row[LRM_MAX_TOPK];
@@ -37,10 +37,9 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
   const int64_t t = blockIdx.x;
   const int tid = threadIdx.x, nt = blockDim.x;
   if (tid < 32) {
-    int r = -1;
+    int64_t r = -1;
     if (tid < k) {
-      r = row_of_pair[t * k + tid];
-      if ((int64_t)r >= cap) r = -1;
+      r = checked_row(row_of_pair[t * k + tid], cap, status);  // outside [-1, cap): flagged, dropped
       s_row[tid] = r;
       s_alpha[tid] = alpha[t * k + tid];
     }
@@ -100,7 +99,7 @@ constexpr int kScatterLoads = 8;
 template <typename T>
 __global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restrict__ row_of_pair,
                                                          const T* __restrict__ dx_c, int64_t n_tok, int k, int H,
-                                                         T* __restrict__ dx) {
+                                                         int64_t cap, T* __restrict__ dx, int32_t* __restrict__ status) {
   chain_wait();
   constexpr int VN = VecTraits<T>::N;
   constexpr int B = kScatterLoads;
@@ -113,7 +112,8 @@ __global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restri
     int base = 0;
     for (int q0 = 0; q0 < ntok * k; q0 += 32) {
       const int q = q0 + lane;
-      const int r = q < ntok * k ? row_of_pair[t0 * k + q] : -1;
+      // a row outside [-1, cap) is flagged and not followed
+      const int r = q < ntok * k ? (int)checked_row(row_of_pair[t0 * k + q], cap, status) : -1;
       const unsigned m = __ballot_sync(0xffffffffu, r >= 0);
       if (r >= 0) s_item[base + __popc(m & ((1u << lane) - 1u))] = make_int2(q / k, r);
       base += __popc(m);
@@ -163,21 +163,21 @@ __global__ void __launch_bounds__(256) scatter_dx_kernel(const int32_t* __restri
 
 void launch_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x, const void* h,
                     const void* phi, int64_t T, int32_t k, int32_t H, int32_t I, lrm_dtype dt, int64_t cap,
-                    void* dy_c, void* x_c, void* h_c, void* phi_c, cudaStream_t s) {
+                    void* dy_c, void* x_c, void* h_c, void* phi_c, int32_t* status, cudaStream_t s) {
   if (T == 0) return;
   if (dt == LRM_BF16) {
     using B = __nv_bfloat16;
     launch_chained(compact_kernel<B>, dim3((unsigned)T), dim3(256), 0, s, row_of_pair, alpha, (const B*)g,
-                   (const B*)x, (const B*)h, (const B*)phi, k, H, I, cap, (B*)dy_c, (B*)x_c, (B*)h_c, (B*)phi_c);
+                   (const B*)x, (const B*)h, (const B*)phi, k, H, I, cap, (B*)dy_c, (B*)x_c, (B*)h_c, (B*)phi_c, status);
   } else {
     launch_chained(compact_kernel<float>, dim3((unsigned)T), dim3(256), 0, s, row_of_pair, alpha, (const float*)g,
                    (const float*)x, (const float*)h, (const float*)phi, k, H, I, cap, (float*)dy_c, (float*)x_c,
-                   (float*)h_c, (float*)phi_c);
+                   (float*)h_c, (float*)phi_c, status);
   }
 }
 
 void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H, lrm_dtype dt,
-                       void* dx, cudaStream_t s) {
+                       int64_t cap, void* dx, int32_t* status, cudaStream_t s) {
   if (T == 0) return;
   const int nvH = H / (dt == LRM_BF16 ? 8 : 4);
   int threads = (nvH + 31) / 32 * 32;  // one thread per 16-byte column slice (warp 0 also builds the list)
@@ -185,10 +185,10 @@ void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, 
   const unsigned blocks = (unsigned)((T + kScatterTok - 1) / kScatterTok);
   if (dt == LRM_BF16)
     launch_chained(scatter_dx_kernel<__nv_bfloat16>, dim3(blocks), dim3(threads), 0, s, row_of_pair,
-                   (const __nv_bfloat16*)dx_c, T, k, H, (__nv_bfloat16*)dx);
+                   (const __nv_bfloat16*)dx_c, T, k, H, cap, (__nv_bfloat16*)dx, status);
   else
     launch_chained(scatter_dx_kernel<float>, dim3(blocks), dim3(threads), 0, s, row_of_pair, (const float*)dx_c, T,
-                   k, H, (float*)dx);
+                   k, H, cap, (float*)dx, status);
 }
 
 }  // namespace lrm

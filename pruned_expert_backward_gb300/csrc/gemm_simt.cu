@@ -23,6 +23,28 @@ constexpr int BM = 64, BN = 64, BK = 16, NT = 256;
 
 enum { EPI_SWIGLU = 0, EPI_STORE = 1 };
 
+// seg_offsets must be a segmentation of [0, seg[E]] within [0, cap]: seg[0] = 0, no decreasing
+// step, seg[E] <= cap.  Checked by every block before it reads a row (block-wide vote); a block
+// that finds it broken records LRM_ERR_BAD_SEGMENTS and computes nothing.
+__device__ bool segments_valid(const int32_t* seg, int E, int64_t cap, int32_t* status) {
+  int ok = 1;
+  for (int e = threadIdx.x; e < E; e += blockDim.x) ok &= seg[e] <= seg[e + 1] ? 1 : 0;
+  if (threadIdx.x == 0) ok &= (seg[0] == 0 && (int64_t)seg[E] <= cap) ? 1 : 0;
+  const bool valid = __syncthreads_and(ok) != 0;
+  if (!valid && threadIdx.x == 0) set_status(status, LRM_ERR_BAD_SEGMENTS);
+  return valid;
+}
+
+// Row of h / phi (pair) or x (token, when div > 0) named by a kept_pair entry u, or -1 when u is
+// outside [0, n_pairs) (recorded as LRM_ERR_BAD_INDEX; the row then reads as zeros).
+__device__ __forceinline__ int64_t gathered_row(int32_t u, int64_t n_pairs, int div, int32_t* status) {
+  if (u < 0 || (int64_t)u >= n_pairs) {
+    set_status(status, LRM_ERR_BAD_INDEX);
+    return -1;
+  }
+  return div > 0 ? u / div : u;
+}
+
 // Map a virtual M-tile id to (expert, first row, end row) from the per-expert tile prefix.
 __device__ __forceinline__ bool find_mtile(const int32_t* seg, int E, int vt, int* s_prefix, int* e_out,
                                            int* r0_out, int* r1_out) {
@@ -54,17 +76,20 @@ __device__ void mtile_prefix(const int32_t* seg, int E, int* s_prefix) {
   __syncthreads();
 }
 
-// C[r, n] = sum_k A[r, k] * B_e[k, n]; A [rows, K] row-major, B_e [K, N] row-major.
-template <typename T, int EPI>
+// C[r, n] = sum_k A[r, k] * B_e[k, n]; A [rows, K] row-major, B_e [K, N] row-major (BT: B_e is
+// stored as [N, K], i.e. C = A B_e^T, as for the rows of W_gate_up).
+template <typename T, int EPI, bool BT = false>
 __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ seg, int E,
                                                   const T* __restrict__ A, const T* __restrict__ B, int K, int N,
                                                   const T* __restrict__ h_c, T* __restrict__ out,
                                                   float* __restrict__ dot_part, int n_part,
-                                                  const int32_t* __restrict__ h_rows) {
+                                                  const int32_t* __restrict__ h_rows, int64_t n_pairs, int64_t cap,
+                                                  int32_t* __restrict__ status) {
   // h_rows (compaction-free variant): the gate/up row of output row r is h_c[h_rows[r]]
   __shared__ int s_prefix[LRM_MAX_EXPERTS + 1];
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
+  if (!segments_valid(seg, E, cap, status)) return;
   mtile_prefix(seg, E, s_prefix);
   int e, r0, r1;
   if (!find_mtile(seg, E, blockIdx.x, s_prefix, &e, &r0, &r1)) return;
@@ -89,7 +114,8 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int n = n0 + nq + q;
-        Bs[kk][nq + q] = (k0 + kk < K && n < N) ? to_f(Be[(int64_t)(k0 + kk) * N + n]) : 0.f;
+        const int64_t bi = BT ? (int64_t)n * K + (k0 + kk) : (int64_t)(k0 + kk) * N + n;
+        Bs[kk][nq + q] = (k0 + kk < K && n < N) ? to_f(Be[bi]) : 0.f;
       }
     }
     __syncthreads();
@@ -118,9 +144,9 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
       if (n >= N) continue;
       if (EPI == EPI_SWIGLU) {
         // N = I here; h_c row is [gate (I) ; up (I)]
-        const int64_t hr = h_rows ? (int64_t)h_rows[r] : (int64_t)r;
-        const float gate = to_f(h_c[hr * 2 * N + n]);
-        const float up = to_f(h_c[hr * 2 * N + N + n]);
+        const int64_t hr = h_rows ? gathered_row(h_rows[r], n_pairs, 0, status) : (int64_t)r;
+        const float gate = hr >= 0 ? to_f(h_c[hr * 2 * N + n]) : 0.f;
+        const float up = hr >= 0 ? to_f(h_c[hr * 2 * N + N + n]) : 0.f;
         const float sg = 1.f / (1.f + expf(-gate));
         const float dphi = acc[i][j];
         const float du = dphi * gate * sg;
@@ -147,11 +173,13 @@ __global__ void __launch_bounds__(NT) varm_kernel(const int32_t* __restrict__ se
 // C_e[m, n] = sum_{r in segment e} A[r, m] * B[r', n]; A [rows, M], B [*, N] row-major, where
 // r' = r, or (compaction-free variant) r' = b_rows[r] / b_div (b_div > 0) or b_rows[r].
 template <typename T>
-__global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ seg, const T* __restrict__ A,
+__global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ seg, int E, const T* __restrict__ A,
                                                   const T* __restrict__ B, int M, int N, float* __restrict__ C,
-                                                  const int32_t* __restrict__ b_rows, int b_div) {
+                                                  const int32_t* __restrict__ b_rows, int b_div, int64_t n_pairs,
+                                                  int64_t cap, int32_t* __restrict__ status) {
   __shared__ float As[BK][BM + 4];
   __shared__ float Bs[BK][BN + 4];
+  if (!segments_valid(seg, E, cap, status)) return;
   const int e = blockIdx.z;
   const int m0 = blockIdx.y * BM, n0 = blockIdx.x * BN;
   const int r0 = seg[e], r1 = seg[e + 1];
@@ -162,12 +190,12 @@ __global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ se
       const int kk = threadIdx.x / 16, q4 = (threadIdx.x % 16) * 4;
       const int r = k0 + kk;
       int64_t rb = r;
-      if (b_rows != nullptr && r < r1) rb = b_div > 0 ? b_rows[r] / b_div : b_rows[r];
+      if (b_rows != nullptr && r < r1) rb = gathered_row(b_rows[r], n_pairs, b_div, status);
 #pragma unroll
       for (int q = 0; q < 4; ++q) {
         const int m = m0 + q4 + q, n = n0 + q4 + q;
         As[kk][q4 + q] = (r < r1 && m < M) ? to_f(A[(int64_t)r * M + m]) : 0.f;
-        Bs[kk][q4 + q] = (r < r1 && n < N) ? to_f(B[rb * N + n]) : 0.f;
+        Bs[kk][q4 + q] = (r < r1 && n < N && rb >= 0) ? to_f(B[rb * N + n]) : 0.f;
       }
     }
     __syncthreads();
@@ -198,6 +226,33 @@ __global__ void __launch_bounds__(NT) vark_kernel(const int32_t* __restrict__ se
   }
 }
 
+// phi_c[r] = SiLU(gate) * up from the row h_c[r] = [gate ; up] (as stored), rows r < seg_offsets[E].
+template <typename T>
+__global__ void __launch_bounds__(256) phi_rows_kernel(const int32_t* __restrict__ seg, int E, int64_t cap, int I,
+                                                       const T* __restrict__ h_c, T* __restrict__ phi_c,
+                                                       int32_t* __restrict__ status) {
+  if (!segments_valid(seg, E, cap, status)) return;
+  int64_t rows = seg[E];
+  if (rows > cap) rows = cap;
+  const int64_t n = rows * I;
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = i / I;
+    const int c = (int)(i - r * I);
+    const float g = to_f(h_c[r * 2 * I + c]), u = to_f(h_c[r * 2 * I + I + c]);
+    phi_c[i] = from_f<T>(g / (1.f + expf(-g)) * u);
+  }
+}
+
+template <typename T>
+void recompute_all(const RecomputeArgs& a, cudaStream_t s) {
+  const int64_t mtiles = (a.cap + BM - 1) / BM + a.E;
+  // h_c = x_c W_gate_up[e]^T over the 2I columns, then phi_c from the stored h_c rows
+  varm_kernel<T, EPI_STORE, true><<<dim3((unsigned)mtiles, (2 * a.I + BN - 1) / BN), NT, 0, s>>>(
+      a.seg_offsets, a.E, (const T*)a.x_c, (const T*)a.w_gate_up, a.H, 2 * a.I, nullptr, (T*)a.h_c, nullptr, 0,
+      nullptr, 0, a.cap, a.status);
+  phi_rows_kernel<T><<<1216, 256, 0, s>>>(a.seg_offsets, a.E, a.cap, a.I, (const T*)a.h_c, (T*)a.phi_c, a.status);
+}
+
 template <typename T>
 void run_all(const GroupedArgs& a, cudaStream_t s) {
   const int E = a.E, H = a.H, I = a.I;
@@ -215,24 +270,31 @@ void run_all(const GroupedArgs& a, cudaStream_t s) {
     const int n_part = (I + BN - 1) / BN;
     varm_kernel<T, EPI_SWIGLU><<<dim3((unsigned)mtiles, n_part), NT, 0, s>>>(
         a.seg_offsets, E, dy, (const T*)a.w_down, H, I, hc, dh, a.row_dot ? a.dot_part : nullptr, n_part,
-        a.kept_pair);
+        a.kept_pair, a.n_pairs, a.cap, a.status);
     if (a.row_dot != nullptr) launch_row_dot(a.dot_part, n_part, a.seg_offsets, E, a.cap, a.row_dot, s);
   }
   // dW_down[e] = dy_c^T phi_c : [H, I]
-  vark_kernel<T><<<dim3((I + BN - 1) / BN, (H + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, dy, pc, H, I,
-                                                                              a.dw_down, a.kept_pair, 0);
+  vark_kernel<T><<<dim3((I + BN - 1) / BN, (H + BM - 1) / BM, E), NT, 0, s>>>(
+      a.seg_offsets, E, dy, pc, H, I, a.dw_down, a.kept_pair, 0, a.n_pairs, a.cap, a.status);
   // dW_gate_up[e] = dh_c^T x_c : [2I, H]
-  vark_kernel<T><<<dim3((H + BN - 1) / BN, (2 * I + BM - 1) / BM, E), NT, 0, s>>>(a.seg_offsets, (const T*)dh, xc,
-                                                                                  2 * I, H, a.dw_gate_up,
-                                                                                  a.kept_pair, a.k);
+  vark_kernel<T><<<dim3((H + BN - 1) / BN, (2 * I + BM - 1) / BM, E), NT, 0, s>>>(
+      a.seg_offsets, E, (const T*)dh, xc, 2 * I, H, a.dw_gate_up, a.kept_pair, a.k, a.n_pairs, a.cap, a.status);
   if (mtiles > 0) {
     // dx_c = dh_c W_gate_up[e] : [R_e, 2I] x [2I, H]
     varm_kernel<T, EPI_STORE><<<dim3((unsigned)mtiles, (H + BN - 1) / BN), NT, 0, s>>>(
-        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx, nullptr, 0, nullptr);
+        a.seg_offsets, E, (const T*)dh, (const T*)a.w_gate_up, 2 * I, H, nullptr, dx, nullptr, 0, nullptr, 0, a.cap,
+        a.status);
   }
 }
 
 }  // namespace
+
+void launch_recompute_simt(const RecomputeArgs& a, lrm_dtype dt, cudaStream_t s) {
+  if (dt == LRM_BF16)
+    recompute_all<__nv_bfloat16>(a, s);
+  else
+    recompute_all<float>(a, s);
+}
 
 void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s) {
   if (dt == LRM_BF16)

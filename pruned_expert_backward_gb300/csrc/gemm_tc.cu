@@ -13,6 +13,10 @@
 //   VM_STORE   dx_c = dh_c[e] W_gate_up[e]         (M = R_e rows, K = 2I, N = H)
 //   VK         dW[e] = A[e]^T B[e] over the segment rows (K = R_e):
 //              dW_down = dy_c^T phi_c, dW_gate_up = dh_c^T x_c; fp32 out
+//   VM_FWD     h_c = x_c[e] W_gate_up[e]^T         (M = R_e rows, K = H, N = 2I), the saved forward
+//              state recomputed for the retained rows: B is K-major (W_gate_up's rows), a pair tile
+//              holds 128 gate columns and the matching 128 up columns, and the epilogue writes h_c
+//              and phi_c = SiLU(gate) * up
 //
 // CTAs run in pairs (a cluster of two) and use the 2-SM MMA: the leader (even) CTA issues
 // tcgen05.mma.cta_group::2, which computes a 256 x 256 tile from both CTAs' shared memory
@@ -89,7 +93,7 @@ static_assert(kSwigluStages < kStages, "the dphi launch's epilogue needs the wid
 constexpr int kTmemCols = 512;
 constexpr uint64_t kWaitNs = 1000000000ull;
 
-enum Kind { VM_SWIGLU = 0, VM_STORE = 1, VK = 2 };
+enum Kind { VM_SWIGLU = 0, VM_STORE = 1, VK = 2, VM_FWD = 3 };
 
 template <bool B>
 struct BoolTag {
@@ -102,7 +106,8 @@ struct TcParams {
   int M, N, K;         // VM: N, K fixed (M per expert); VK: M, N fixed (K per expert)
   int nM, nN;          // tile counts along the fixed dims (VK: nM and nN; VM: nN)
   const int32_t* seg;  // [E+1]
-  const int32_t* plan; // [E+1] m-tile prefix (VM), then [E] experts by R_e descending (VK)
+  const int32_t* plan; // [E+1] m-tile prefix (VM), then [E] experts by R_e descending (VK), then
+                       // the segment check word (1: seg_offsets valid; 0: run no tile)
   void* out;           // VM_SWIGLU: dh_c [rows, 2N]; VM_STORE: dx_c [rows, N]; VK: fp32 [E, M, N]
   const __nv_bfloat16* h_c;  // VM_SWIGLU: [rows, 2N]
   int32_t* status;
@@ -127,7 +132,18 @@ struct TcParams {
   // VM, compacted rows: epilogue through TMA.  maps_a then holds the per-expert output maps
   // (dh_c viewed as [rows][2][I], dx_c as [rows][H]), and tmC the gate/up map of h_c ([rows][2][I]).
   int tma_epi;
+  int gP;  // gather mode: pairs in h / phi (T*k); a kept_pair entry outside [0, gP) is not followed
 };
+
+// Pair named by kept_pair for a gathered row: in [0, gP), or -1 (flagged; the row reads as zeros).
+__device__ __forceinline__ int gather_pair(const TcParams& p, int r) {
+  const int u = __ldg(p.kept_pair + r);
+  if (u < 0 || u >= p.gP) {
+    set_status(p.status, LRM_ERR_BAD_INDEX);
+    return -1;
+  }
+  return u;
+}
 
 // ---------------------------------------------------------------- PTX wrappers -------
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
@@ -221,24 +237,24 @@ __device__ __forceinline__ void mbar_expect_tx_cluster(uint32_t cbar, uint32_t b
 // TMA load into this CTA's shared memory that completes on an mbarrier of either CTA of the pair.
 __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
-      "%3}], [%4];" ::"r"(dst),
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(cbar)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                                  uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
-      "%3, %4}], [%5];" ::"r"(dst),
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(cbar)
       : "memory");
 }
 __device__ __forceinline__ void tma_load_4d_pair(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2, int c3,
                                                  uint32_t cbar) {
   asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 [%0], [%1, {%2, "
-      "%3, %4, %5}], [%6];" ::"r"(dst),
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.cta_group::2 "
+      "[%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(cbar)
       : "memory");
 }
@@ -358,7 +374,9 @@ struct Tile {
 };
 
 // The tile tables (seg_offsets and the plan) are tiny and read through the read-only cache.
+// Segments that failed the plan kernel's check give no tile at all.
 __device__ __forceinline__ int total_tiles(const TcParams& p) {
+  if (__ldg(p.plan + 2 * p.E + 1) != 1) return 0;
   return p.kind == VK ? p.E * ((p.nM + 1) / 2) * p.nN : __ldg(p.plan + p.E) * p.nN;
 }
 
@@ -388,7 +406,7 @@ __device__ __forceinline__ Tile decode(const TcParams& p, int t, int rank) {
     d.row0 = __ldg(p.seg + lo) + (mg - __ldg(p.plan + lo)) * (2 * kBM) + rank * kBM;
     d.row_end = min(seg_end, d.row0 + kBM);
     d.m0 = 0;
-    d.n0 = nt * kBN;
+    d.n0 = nt * (p.kind == VM_FWD ? kBN / 2 : kBN);  // VM_FWD: 128 gate (and 128 up) columns
     d.k_iters = (p.K + kBK - 1) / kBK;
     d.has_rows = d.row0 < seg_end;
   }
@@ -473,8 +491,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pairs named by kept_pair for K rows r0 + lane and r0 + 32 + lane of a slice (-1 past the segment)
     auto load_idx = [&](const Tile& dd, int kbb, int& u0, int& u1) {
       const int r0 = dd.row0 + kbb * kBK;
-      u0 = r0 + lane < dd.row_end ? __ldg(p.kept_pair + r0 + lane) : -1;
-      u1 = r0 + 32 + lane < dd.row_end ? __ldg(p.kept_pair + r0 + 32 + lane) : -1;
+      u0 = r0 + lane < dd.row_end ? gather_pair(p, r0 + lane) : -1;
+      u1 = r0 + 32 + lane < dd.row_end ? gather_pair(p, r0 + 32 + lane) : -1;
     };
     int t = pair, kb = 0;
     Tile d{};
@@ -599,6 +617,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               tma_load_2d_pair(b_dst, mb, nb, r, fb);
               tma_load_2d_pair(b_dst + 8192, mb, nb + 64, r, fb);
             }
+          } else if (p.kind == VM_FWD) {
+            if (d.has_rows) tma_load_2d_pair(a_dst, &tmA, kb * kBK, d.row0, fb);
+            // this CTA's 128 B rows (K-major): the expert's gate rows n0.. (leader) or its up rows
+            // I + n0.. (the other CTA), so that the pair tile's columns are gate then matching up
+            tma_load_3d_pair(b_dst, &tmB, kb * kBK, (rank == 0 ? 0 : p.N) + d.n0, d.e, fb);
           } else {
             if (d.has_rows) tma_load_2d_pair(a_dst, &tmA, kb * kBK, d.row0, fb);
             if (p.merged_b) {
@@ -619,13 +642,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     // Only the leader issues: tcgen05.mma.cta_group::2 computes the 256 x 256 pair tile from
     // both CTAs' shared memory into both CTAs' TMEM (128 rows each).
     if (leader && lane == 0) {
-      const uint32_t idesc = instr_desc(p.kind == VK ? 1u : 0u, 1u);
+      const bool b_kmajor = p.kind == VM_FWD;  // W_gate_up's rows, K contiguous
+      const uint32_t idesc = instr_desc(p.kind == VK ? 1u : 0u, b_kmajor ? 0u : 1u);
       // descriptors of stage 0; a stage or a 16-deep K step is a constant offset in the address
       // field (addresses stay below 256 KB, so the 14-bit field never carries)
       const uint32_t a0 = smem_u32(smem), b0 = a0 + kABytes;
       const uint64_t adesc0 = p.kind == VK ? smem_desc(a0, 8192, 1024) : smem_desc(a0, 16, 1024);
-      const uint64_t bdesc0 = smem_desc(b0, 8192, 1024);
-      const uint64_t a_kstep = p.kind == VK ? (2048 >> 4) : (32 >> 4), b_kstep = 2048 >> 4;
+      const uint64_t bdesc0 = b_kmajor ? smem_desc(b0, 16, 1024) : smem_desc(b0, 8192, 1024);
+      const uint64_t a_kstep = p.kind == VK ? (2048 >> 4) : (32 >> 4);
+      const uint64_t b_kstep = b_kmajor ? (32 >> 4) : (2048 >> 4);
       // the issue loop, compiled once per kind of B delivery (the loop is on the critical path)
       auto issue = [&](auto gather_tag) {
         constexpr bool G = decltype(gather_tag)::value;
@@ -693,6 +718,82 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
     // drain: all MMAs writing this CTA's TMEM complete before it is released
     mbar_wait(drain, 0, abortv, p.status, false);
+  } else if (warp >= 2 && warp < first_extra && p.kind == VM_FWD) {
+    // ---------------------------------------------- epilogue, recomputed forward state ------
+    // The pair tile's 256 accumulator columns are 128 gate columns (the leader's B rows) and then
+    // the 128 matching up columns (the other CTA's).  Warp w reads TMEM lanes 32*(w%4) .. +31 (one
+    // row per lane) and takes 64 of the gate columns with their up columns, 32 at a time: gate and
+    // up are rounded to bf16 (the h row the forward stores), phi = SiLU(gate) * up is formed from
+    // the rounded values as the forward's SwiGLU does, and the three 32 x 32 bf16 boxes (64-byte
+    // swizzle) leave by TMA stores through the expert's maps (h_c as [rows][2][I], phi_c as
+    // [rows][I]), whose row extent ends at the segment end.
+    const int ew = warp - 2, q = warp & 3, half = ew >> 2;
+    uint8_t* wbuf = epi + ew * epi_bytes<S>();
+    const uint32_t wbuf_s = smem_u32(wbuf);
+    const int swz = (lane >> 1) & 3;
+    int last_e = -1;
+    bool ok = true;
+    int lt = 0;
+    for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+      const Tile d = decode(p, t, rank);
+      const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
+      const int row_base = d.row0 + q * 32;
+      const int nrows = d.has_rows ? min(32, d.row_end - row_base) : 0;
+      const CUtensorMap* hmap = p.maps_a + d.e;
+      const CUtensorMap* fmap = p.maps_b + d.e;
+      if (lane == 0 && nrows > 0 && d.e != last_e) {
+        tensormap_acquire(hmap);
+        tensormap_acquire(fmap);
+        last_e = d.e;
+      }
+      if (!mbar_wait(accf0 + 8 * acc, acc_ph, abortv, p.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + acc * kBN + ((uint32_t)(q * 32) << 16);
+      for (int c2 = 0; c2 < 2 && nrows > 0; ++c2) {
+        const int cc = half * 64 + c2 * 32;  // gate column within the tile
+        const int col = d.n0 + cc;           // column of h's gate half and of phi
+        if (col >= p.N) break;               // warp-uniform
+        uint32_t vg[32], vu[32];
+        tmem_ld32(tbase + cc, vg);
+        tmem_ld32(tbase + kBN / 2 + cc, vu);
+        if (lane == 0) bulk_wait_read_all();  // the previous chunk's stores have read the boxes
+        __syncwarp();
+        uint8_t* grow = wbuf + lane * 64;
+        uint8_t* urow = grow + kVmBoxBytes;
+        uint8_t* frow = grow + 2 * kVmBoxBytes;
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          float gf[8], uf[8], fo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            gf[i] = __uint_as_float(vg[8 * jj + i]);
+            uf[i] = __uint_as_float(vu[8 * jj + i]);
+          }
+          const uint4 gq = pack(gf), uq = pack(uf);  // the stored gate / up values
+          unpack(gq, gf);
+          unpack(uq, uf);
+#pragma unroll
+          for (int i = 0; i < 8; ++i) fo[i] = gf[i] / (1.f + expf(-gf[i])) * uf[i];
+          *reinterpret_cast<uint4*>(grow + ((jj ^ swz) << 4)) = gq;
+          *reinterpret_cast<uint4*>(urow + ((jj ^ swz) << 4)) = uq;
+          *reinterpret_cast<uint4*>(frow + ((jj ^ swz) << 4)) = pack(fo);
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(hmap, wbuf_s, col, 0, row_base);
+          tma_store_3d(hmap, wbuf_s + kVmBoxBytes, col, 1, row_base);
+          tma_store_2d(fmap, wbuf_s + 2 * kVmBoxBytes, col, row_base);
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(acce_lead + 8 * acc);
+    }
+    if (lane == 0) bulk_wait_all();  // stores complete before the CTA exits
   } else if (warp >= 2 && warp < first_extra && p.kind != VK && p.tma_epi) {
     // ---------------------------------------------------- epilogue, var-M through TMA -------
     // Warp w reads TMEM lanes 32*(w%4) .. +31 (tile rows q*32 .. +31) and half of the 256 columns,
@@ -846,9 +947,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         // while the tile's MMAs run, pull this warp's gate and up rows (its 128 columns of
         // each) into L2, so that the SwiGLU epilogue below reads them from L2
         const int I = p.N, col = d.n0 + half * 128;
-        const __nv_bfloat16* hrow = p.kept_pair ? p.gsrc + (int64_t)__ldg(p.kept_pair + row_base + lane) * 2 * I
-                                                : p.h_c + (int64_t)(row_base + lane) * 2 * I;
-        if (col < I) {
+        const int64_t hr = p.kept_pair ? (int64_t)gather_pair(p, row_base + lane) : (int64_t)(row_base + lane);
+        const __nv_bfloat16* hrow = (p.kept_pair ? p.gsrc : p.h_c) + hr * 2 * I;
+        if (col < I && hr >= 0) {
 #pragma unroll
           for (int b = 0; b < 2; ++b) {
             if (col + b * 64 >= I) break;
@@ -908,11 +1009,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               const int rr = i * 8 + sub;
               if (rr < nrows && col < I) {
                 // gate/up row: the compacted row, or (compaction-free) the pair's row of h
-                const __nv_bfloat16* hrow =
-                    p.kept_pair ? p.gsrc + (int64_t)__ldg(p.kept_pair + row_base + rr) * 2 * I
-                                : p.h_c + (int64_t)(row_base + rr) * 2 * I;
-                gv[i] = ldg16(hrow + col);
-                uv[i] = ldg16(hrow + I + col);
+                const int64_t hr =
+                    p.kept_pair ? (int64_t)gather_pair(p, row_base + rr) : (int64_t)(row_base + rr);
+                const __nv_bfloat16* hrow = (p.kept_pair ? p.gsrc : p.h_c) + hr * 2 * I;
+                gv[i] = hr >= 0 ? ldg16(hrow + col) : make_uint4(0, 0, 0, 0);
+                uv[i] = hr >= 0 ? ldg16(hrow + I + col) : make_uint4(0, 0, 0, 0);
               }
             }
 #pragma unroll
@@ -981,7 +1082,11 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Tile tables from seg_offsets: plan[0..E] = exclusive prefix of ceil(R_e / 256) (var-M pair tiles),
-// plan[E+1 .. 2E] = experts ordered by R_e descending, ties by expert id (var-K, longest first).
+// plan[E+1 .. 2E] = experts ordered by R_e descending, ties by expert id (var-K, longest first),
+// plan[2E+1] = 1 if seg_offsets is a segmentation of [0, seg_offsets[E]] within [0, cap]
+// (seg_offsets[0] = 0, no decreasing step, seg_offsets[E] <= cap), else 0: then
+// LRM_ERR_BAD_SEGMENTS is recorded and the GEMM launches run no tile (total_tiles), so no map
+// built from the bad offsets is ever used.
 // maps[j][e] = template j with its row extent cut at seg_offsets[e+1] (var-K operands, var-M outputs).
 // Templates 0-3: var-K operands (row extent is dimension 1); 4: dh_c as [rows][2][I] (rows are
 // dimension 2); 5: dx_c as [rows][H] (dimension 1).
@@ -989,14 +1094,24 @@ constexpr int kMapSets = 6;
 struct MapTemplates {
   CUtensorMap t[kMapSets];
 };
-__global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict__ seg, int E,
+__global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict__ seg, int E, int64_t cap,
                                                        int32_t* __restrict__ plan, CUtensorMap* __restrict__ maps,
-                                                       const __grid_constant__ MapTemplates tpl) {
+                                                       const __grid_constant__ MapTemplates tpl,
+                                                       int32_t* __restrict__ status) {
   chain_wait();
   __shared__ int s_r[LRM_MAX_EXPERTS];
   __shared__ int warp_tot[32];
   const int e = threadIdx.x;
-  const int r = e < E ? seg[e + 1] - seg[e] : 0;
+  bool good = true;
+  if (e < E) good = seg[e] <= seg[e + 1];
+  if (e == 0) good = good && seg[0] == 0;
+  if (e == E - 1) good = good && (int64_t)seg[E] <= cap;
+  const bool valid = __syncthreads_and(good ? 1 : 0) != 0;
+  if (e == 0) {
+    plan[2 * E + 1] = valid ? 1 : 0;
+    if (!valid) set_status(status, LRM_ERR_BAD_SEGMENTS);
+  }
+  const int r = e < E && valid ? seg[e + 1] - seg[e] : 0;
   if (e < E) s_r[e] = r;
   const int mt = (r + 2 * kBM - 1) / (2 * kBM);
   // exclusive block scan of mt
@@ -1034,7 +1149,7 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
   // one (template, expert) map per thread
   for (int i = threadIdx.x; i < kMapSets * E; i += blockDim.x) {
     const int j = i / E, ee = i - j * E;
-    const uint32_t rows_end = (uint32_t)max(1, seg[ee + 1]);
+    const uint32_t rows_end = valid ? (uint32_t)max(1, seg[ee + 1]) : 1u;
     {
       CUtensorMap* dst = maps + j * E + ee;
       const uint4* src = reinterpret_cast<const uint4*>(&tpl.t[j]);
@@ -1128,6 +1243,16 @@ bool make_map_blocks_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t K
   const cuuint32_t box[4] = {64, 64, 2, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+// bf16 [E, rows, K] (K contiguous: the rows of W_gate_up) with a {64, 128, 1} box, 128-byte swizzle.
+bool make_map_kmajor_3d(CUtensorMap* m, const void* base, uint64_t E, uint64_t rows, uint64_t K) {
+  const cuuint64_t dims[3] = {K, rows, E};
+  const cuuint64_t strides[2] = {K * 2, rows * K * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  return encode_fn()(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                      CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -1230,11 +1355,36 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
 lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                       int64_t tiles_bound, cudaStream_t s) {
   if (tiles_bound <= 0) return LRM_OK;
-  return p.kind == VM_SWIGLU ? launch_stages<kSwigluStages>(a, b, c, p, tiles_bound, s)
-                             : launch_stages<kStages>(a, b, c, p, tiles_bound, s);
+  // dphi + SwiGLU and the recomputed forward state need the wide per-warp epilogue buffers
+  return p.kind == VM_SWIGLU || p.kind == VM_FWD ? launch_stages<kSwigluStages>(a, b, c, p, tiles_bound, s)
+                                                 : launch_stages<kStages>(a, b, c, p, tiles_bound, s);
 }
 
 }  // namespace
+
+lrm_status launch_recompute_tc(const RecomputeArgs& g, const GemmWs& ws, cudaStream_t s) {
+  if (!device_ok() || encode_fn() == nullptr) return LRM_ERR_UNSUPPORTED;
+  const int E = g.E, H = g.H, I = g.I;
+  const uint64_t rows = g.cap > 0 ? (uint64_t)g.cap : 1;
+  int32_t* plan = ws.plan;
+  CUtensorMap* maps = static_cast<CUtensorMap*>(ws.maps);
+  // per-expert output maps: set 4 = h_c as [rows][2][I], set 5 = phi_c as [rows][I] (the plan
+  // kernel cuts both at the segment end); sets 0-3 are not used here and only need to be valid
+  MapTemplates tpl;
+  if (!make_map_halves(&tpl.t[4], g.h_c, rows, I) || !make_map_rows32(&tpl.t[5], g.phi_c, rows, I))
+    return LRM_ERR_CUDA;
+  for (int j = 0; j < 4; ++j) tpl.t[j] = tpl.t[5];
+  launch_chained(tc_plan_kernel, dim3(1), dim3(1024), 0, s, g.seg_offsets, E, g.cap, plan, maps, tpl, g.status);
+  if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
+  CUtensorMap mA, mB;
+  if (!make_map_2d(&mA, g.x_c, rows, H, kBM) || !make_map_kmajor_3d(&mB, g.w_gate_up, E, 2 * (uint64_t)I, H))
+    return LRM_ERR_CUDA;
+  TcParams p{VM_FWD, E, 0, I, H, 0, (I + kBN / 2 - 1) / (kBN / 2), g.seg_offsets, plan, nullptr, nullptr, g.status,
+             maps + 4 * E, maps + 5 * E};
+  p.tma_epi = 1;
+  const int64_t vm_bound = ((int64_t)g.cap + 2 * kBM - 1) / (2 * kBM) + E;
+  return launch_one(mA, mB, mA, p, vm_bound * p.nN, s);
+}
 
 lrm_status launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s) {
   wait_selftest_kernel<<<1, 32, 0, s>>>(status, (uint64_t)limit_ns);
@@ -1245,7 +1395,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   if (!device_ok() || encode_fn() == nullptr) return LRM_ERR_UNSUPPORTED;
   const int E = g.E, H = g.H, I = g.I;
   const uint64_t rows = g.cap > 0 ? (uint64_t)g.cap : 1;
-  int32_t* plan = ws.plan;  // [2E+1] tile tables
+  int32_t* plan = ws.plan;  // [2E+2] tile tables and the segment check word
   CUtensorMap* maps = static_cast<CUtensorMap*>(ws.maps);
   MapTemplates tpl;
   const bool gather = g.kept_pair != nullptr;  // compaction-free: phi / x rows gathered by index
@@ -1269,7 +1419,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
     *merged_b = mergeable(N) && make_map_blocks_3d(m, base, E, K, N);
     return *merged_b || make_map_3d(m, base, E, K, N);
   };
-  launch_chained(tc_plan_kernel, dim3(1), dim3(1024), 0, s, g.seg_offsets, E, plan, maps, tpl);
+  launch_chained(tc_plan_kernel, dim3(1), dim3(1024), 0, s, g.seg_offsets, E, g.cap, plan, maps, tpl, g.status);
   if (cudaGetLastError() != cudaSuccess) return LRM_ERR_CUDA;
 
   CUtensorMap mA, mB;
@@ -1281,7 +1431,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   using B16 = const __nv_bfloat16*;
   TcParams p{VM_SWIGLU, E, 0, I, H, 0, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dh_c,
              (B16)g.h_c, g.status, maps + 4 * E, nullptr, g.dot_part, (I + 127) / 128,
-             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I, 0, vm_merged, tma_epi};
+             g.kept_pair, gather ? (B16)g.h : nullptr, 0, 2 * I, 0, vm_merged, tma_epi, (int)g.n_pairs};
   CUtensorMap mH = mA;  // gate/up tiles of h_c for the TMA epilogue
   if (tma_epi && !make_map_halves(&mH, g.h_c, rows, I)) return LRM_ERR_CUDA;
   if ((st = launch_one(mA, mB, mH, p, vm_bound * p.nN, s))) return st;
@@ -1289,7 +1439,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   // dW_down[e] = dy_c^T phi_c  (M = H, N = I)
   p = TcParams{VK, E, H, I, 0, (H + kBM - 1) / kBM, (I + kBN - 1) / kBN, g.seg_offsets, plan, g.dw_down,
                nullptr, g.status, maps + 0 * E, maps + 1 * E, nullptr, 0,
-               g.kept_pair, gather ? (B16)g.phi : nullptr, 0, I, merged[0], merged[1]};
+               g.kept_pair, gather ? (B16)g.phi : nullptr, 0, I, merged[0], merged[1], 0, (int)g.n_pairs};
   mA = tpl.t[0];
   mB = tpl.t[1];
   CUtensorMap mC;
@@ -1298,7 +1448,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
   p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
                g.dw_gate_up, nullptr, g.status, maps + 2 * E, maps + 3 * E, nullptr, 0,
-               g.kept_pair, gather ? (B16)g.x : nullptr, g.k, H, merged[2], merged[3]};
+               g.kept_pair, gather ? (B16)g.x : nullptr, g.k, H, merged[2], merged[3], 0, (int)g.n_pairs};
   mA = tpl.t[2];
   mB = tpl.t[3];
   if (!make_map_out3d(&mC, g.dw_gate_up, E, 2 * I, H)) return LRM_ERR_CUDA;

@@ -26,9 +26,10 @@ struct SelectWs {
 // Scratch of the tensor-core grouped GEMMs: tile tables, then 6*E per-expert TMA tensor maps
 // (128 bytes each, 128-byte aligned) built on the device from seg_offsets.
 struct GemmWs {
-  int32_t* plan;  // [2E+1]
+  int32_t* plan;  // [2E+2]
   void* maps;     // [6][E] CUtensorMap
 };
+size_t gemm_plan_bytes(int32_t E);  // plan[2E+2]: tile tables and the segment-check word
 size_t gemm_ws_bytes(int32_t E);
 
 struct WsLayout {
@@ -62,10 +63,10 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
 
 void launch_compact(const int32_t* row_of_pair, const float* alpha, const void* g, const void* x, const void* h,
                     const void* phi, int64_t T, int32_t k, int32_t H, int32_t I, lrm_dtype dt, int64_t cap,
-                    void* dy_c, void* x_c, void* h_c, void* phi_c, cudaStream_t s);
+                    void* dy_c, void* x_c, void* h_c, void* phi_c, int32_t* status, cudaStream_t s);
 
 void launch_scatter_dx(const int32_t* row_of_pair, const void* dx_c, int64_t T, int32_t k, int32_t H, lrm_dtype dt,
-                       void* dx, cudaStream_t s);
+                       int64_t cap, void* dx, int32_t* status, cudaStream_t s);
 
 struct GroupedArgs {
   const int32_t* seg_offsets;
@@ -82,6 +83,7 @@ struct GroupedArgs {
   const int32_t* kept_pair;
   int32_t k;
   const void *x, *h, *phi;
+  int64_t n_pairs;  // T*k: rows of h and phi; a kept_pair entry outside [0, n_pairs) is not followed
 };
 
 // Parts of the dphi . phi row sums: one per 128 output columns (tensor-core path) or per 64
@@ -93,6 +95,18 @@ void launch_router_grad(const int32_t* row_of_pair, const float* alpha, const fl
                         int64_t cap, float* dalpha, cudaStream_t s);
 
 void launch_grouped_simt(const GroupedArgs& a, lrm_dtype dt, cudaStream_t s);
+
+// The saved forward state of the retained rows, recomputed from x_c (lrm_recompute_forward).
+struct RecomputeArgs {
+  const int32_t* seg_offsets;
+  const void *x_c, *w_gate_up;
+  int32_t E, H, I;
+  int64_t cap;
+  void *h_c, *phi_c;
+  int32_t* status;
+};
+lrm_status launch_recompute_tc(const RecomputeArgs& a, const GemmWs& ws, cudaStream_t s);
+void launch_recompute_simt(const RecomputeArgs& a, lrm_dtype dt, cudaStream_t s);
 // Returns LRM_OK, or LRM_ERR_UNSUPPORTED / LRM_ERR_CUDA when the tensor-core path cannot run.
 lrm_status launch_grouped_tc(const GroupedArgs& a, const GemmWs& ws, cudaStream_t s);
 lrm_status launch_wait_selftest(int32_t* status, int64_t limit_ns, cudaStream_t s);

@@ -182,8 +182,10 @@ __global__ void __launch_bounds__(kSelChunk) sel_bucket_kernel(
   if (valid && !good) row_of_pair[u] = -1;
   if (good) {
     const int pos = s_base[e_raw] + s_wcnt[warp * E + e_raw] + rank_w;
-    sorted_u[pos] = (int32_t)u;
-    sorted_key[pos] = key;
+    if (LRM_DCHECK(pos >= 0 && pos < P, status, LRM_ERR_BAD_INDEX)) {
+      sorted_u[pos] = (int32_t)u;
+      sorted_key[pos] = key;
+    }
   }
 }
 
@@ -229,7 +231,8 @@ __device__ __forceinline__ int warp_excl_scan(int v, int* total, int* sm) {
 __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
     const int32_t* __restrict__ bucket_start, const int32_t* __restrict__ keep_arr,
     const int32_t* __restrict__ seg_offsets, const int32_t* __restrict__ sorted_u, uint32_t* sorted_key,
-    int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair, int direct) {
+    int32_t* __restrict__ kept_pair, int32_t* __restrict__ row_of_pair, int direct, int64_t P, int64_t cap,
+    int32_t* __restrict__ status) {
   chain_wait();
   extern __shared__ uint32_t s_dyn[];
   int* hist = reinterpret_cast<int*>(s_dyn);  // [kExpBins]
@@ -249,6 +252,7 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
   if (keep >= load) {
     for (int i = tid; i < load; i += kExpThreads) {
       const int u = bu[i];
+      if (!LRM_DCHECK(u >= 0 && u < P && base + i < cap, status, LRM_ERR_BAD_INDEX)) continue;
       kept_pair[base + i] = u;
       if (direct) row_of_pair[u] = base + i;
       else bk[i] = (uint32_t)(base + i);
@@ -257,8 +261,11 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
   }
   if (keep <= 0) {
     for (int i = tid; i < load; i += kExpThreads) {
-      if (direct) row_of_pair[bu[i]] = -1;
-      else bk[i] = 0xffffffffu;
+      if (direct) {
+        if (LRM_DCHECK(bu[i] >= 0 && bu[i] < P, status, LRM_ERR_BAD_INDEX)) row_of_pair[bu[i]] = -1;
+      } else {
+        bk[i] = 0xffffffffu;
+      }
     }
     return;
   }
@@ -368,7 +375,8 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
           int off = 0;
           if (lane == 0 && bal) off = atomicAdd(&s_fill, __popc(bal));
           off = __shfl_sync(0xffffffffu, off, 0);
-          if (m) s_cand[off + __popc(bal & ((1u << lane) - 1u))] = keys[q];
+          const int slot = off + __popc(bal & ((1u << lane) - 1u));
+          if (m && LRM_DCHECK(slot < kExpCandCap, status, LRM_ERR_BAD_INDEX)) s_cand[slot] = keys[q];
         }
         __syncthreads();
       }
@@ -422,9 +430,11 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
       if (i < load) {
         const bool kept = (kfm[q] >> lane) & 1u;
         const int r = kept ? base + pos + __popc(kfm[q] & lt_mask) : -1;
-        if (kept) kept_pair[r] = bu[i];
-        if (direct) row_of_pair[bu[i]] = r;
-        else bk[i] = (uint32_t)r;
+        if (LRM_DCHECK(bu[i] >= 0 && bu[i] < P && r < cap, status, LRM_ERR_BAD_INDEX)) {
+          if (kept) kept_pair[r] = bu[i];
+          if (direct) row_of_pair[bu[i]] = r;
+          else bk[i] = (uint32_t)r;
+        }
       }
       pos += __popc(kfm[q]);
     }
@@ -437,11 +447,14 @@ __global__ void __launch_bounds__(kExpThreads) sel_expert_kernel(
 __global__ void __launch_bounds__(256) sel_rows_kernel(const int32_t* __restrict__ bucket_start, int E,
                                                        const int32_t* __restrict__ sorted_u,
                                                        const uint32_t* __restrict__ slot_row,
-                                                       int32_t* __restrict__ row_of_pair) {
+                                                       int32_t* __restrict__ row_of_pair, int64_t P,
+                                                       int32_t* __restrict__ status) {
   chain_wait();
   const int64_t n = bucket_start[E];
-  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x)
-    row_of_pair[sorted_u[i]] = (int32_t)slot_row[i];
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += (int64_t)gridDim.x * blockDim.x) {
+    const int32_t u = sorted_u[i];
+    if (LRM_DCHECK(u >= 0 && u < P, status, LRM_ERR_BAD_INDEX)) row_of_pair[u] = (int32_t)slot_row[i];
+  }
 }
 
 // From this many pairs on, the rows are scattered by sel_rows_kernel (one launch more; the
@@ -468,12 +481,12 @@ void launch_select(const int32_t* topk_idx, const float* scores, const int32_t* 
     const bool direct = P < kDeferRowsMinPairs;
     launch_chained(sel_expert_kernel, dim3(E), dim3(kExpThreads), (size_t)smem, s, (const int32_t*)ws.bucket_start,
                    (const int32_t*)ws.keep, (const int32_t*)seg_offsets, (const int32_t*)ws.sorted_u, ws.sorted_key,
-                   kept_pair, row_of_pair, direct ? 1 : 0);
+                   kept_pair, row_of_pair, direct ? 1 : 0, P, cap, status);
     if (!direct) {
       const int64_t blocks = (P + 255) / 256;
       launch_chained(sel_rows_kernel, dim3((unsigned)(blocks < 1216 ? blocks : 1216)), dim3(256), 0, s,
                      (const int32_t*)ws.bucket_start, E, (const int32_t*)ws.sorted_u, (const uint32_t*)ws.sorted_key,
-                     row_of_pair);
+                     row_of_pair, P, status);
     }
   }
 }

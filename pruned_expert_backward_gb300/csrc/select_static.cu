@@ -8,11 +8,16 @@
 // is part of the library image on every GPU that loads it (about 12 MB, held until exit).
 //
 // Set-up: the first call on a device (with that device current) looks up the array's
-// device address with cudaGetSymbolAddress and keeps it; later calls on that device reuse
-// it.  Make that first call on each device before any stream capture.
+// device address with cudaGetSymbolAddress and keeps it, together with the unique id of the
+// CUDA context it belongs to; later calls on that device reuse it while the context is the
+// same.  A cudaDeviceReset destroys the primary context (and the array's address with it):
+// the next call sees a new context id and looks the address up again.  Make the first call
+// on each device, and the first call after a reset, before any stream capture.
 // Sharing: every call uses the same array and leaves its contents behind.  No word of it has
 // to start at zero (each call writes everything it reads first), but two calls that overlap
 // on the GPU (different streams or threads without ordering between them) race on it.
+#include <cuda.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -37,16 +42,49 @@ static __device__ __align__(256) unsigned char g_select_scratch[kStaticBytes];
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 void* g_scratch_ptr[kMaxDevices] = {};
+unsigned long long g_scratch_ctx[kMaxDevices] = {};
 
-// Device address of the array on the current device (set up on first use), or nullptr.
+typedef CUresult (*CtxGetCurrentFn)(CUcontext*);
+typedef CUresult (*CtxGetIdFn)(CUcontext, unsigned long long*);
+
+// Unique id of the current CUDA context (0 if the driver cannot say), through driver entry
+// points fetched by the runtime.
+unsigned long long current_context_id() {
+  static CtxGetCurrentFn get_current = nullptr;
+  static CtxGetIdFn get_id = nullptr;
+  static bool tried = false;
+  if (!tried) {
+    tried = true;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      get_id = reinterpret_cast<CtxGetIdFn>(p);
+  }
+  CUcontext ctx = nullptr;
+  unsigned long long id = 0;
+  if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr ||
+      get_id(ctx, &id) != CUDA_SUCCESS)
+    return 0;
+  return id;
+}
+
+// Device address of the array on the current device, looked up on the first call in each CUDA
+// context of that device (0: the context id is unknown, so it is looked up on every call), or
+// nullptr.
 void* scratch_for_current_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return nullptr;
+  unsigned long long ctx = current_context_id();  // 0 before the runtime has made a context current
   std::lock_guard<std::mutex> lock(g_mu);
-  if (g_scratch_ptr[dev] == nullptr) {
+  if (g_scratch_ptr[dev] == nullptr || ctx == 0 || ctx != g_scratch_ctx[dev]) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_select_scratch) != cudaSuccess) return nullptr;
     g_scratch_ptr[dev] = p;
+    g_scratch_ctx[dev] = current_context_id();  // the look-up has made the primary context current
   }
   return g_scratch_ptr[dev];
 }
@@ -61,8 +99,10 @@ extern "C" lrm_status lrm_select_static(const int32_t* topk_idx, const float* sc
                                         int64_t T, int32_t k, int32_t E, int64_t cap, int32_t* seg_offsets,
                                         int32_t* kept_pair, int32_t* row_of_pair, int32_t* dev_status,
                                         cudaStream_t stream) {
+  LRM_NVTX_RANGE();
   if (T < 0 || k < 1 || E < 1) return LRM_ERR_INVALID_ARG;
   if (k > LRM_MAX_TOPK || E > LRM_MAX_EXPERTS) return LRM_ERR_SHAPE;
+  if (T > kStaticMaxPairs / k) return LRM_ERR_SHAPE;  // tested before forming T*k
   const int64_t P = T * (int64_t)k;
   if (P > kStaticMaxPairs) return LRM_ERR_SHAPE;  // beyond the fixed scratch: use lrm_select
   if (cap < 0 || cap > INT32_MAX) return LRM_ERR_INVALID_ARG;

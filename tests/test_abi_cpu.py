@@ -27,7 +27,7 @@ def test_library_exports_every_declared_symbol():
 
 def test_status_strings():
     lib = ensure_built()
-    for code in range(0, 11):
+    for code in range(0, 12):
         assert lib.lrm_status_string(code)
     assert lib.lrm_status_string(99) == b"unknown status"
 
@@ -46,8 +46,10 @@ def test_workspace_size_and_host_validation():
     assert lib.lrm_score(None, None, None, 16, 2, 64, 32, 0, None, None, None) == 1
     assert lib.lrm_select(None, None, None, 16, 2, 4, 32, None, None, None, None, 0, None, None) == 1
     assert lib.lrm_compact(None, None, None, None, None, None, 16, 2, 64, 32, 0, 32, None, None, None, None,
-                           None) == 1
-    assert lib.lrm_scatter_dx(None, None, 16, 2, 64, 0, None, None) == 1
+                           None, None) == 1
+    assert lib.lrm_scatter_dx(None, None, 16, 2, 64, 0, 32, None, None, None) == 1
+    fake16 = C.c_void_p(0x1000)
+    assert lib.lrm_scatter_dx(fake16, fake16, 16, 2, 64, 0, -1, fake16, None, None) == 1  # negative cap
     assert lib.lrm_plan_quotas(None, 16, 2, 4, 0, 8, 10, 0, None, None, None, None, None) == 1
     # unknown GEMM flag
     fake = C.c_void_p(0x1000)
@@ -86,3 +88,19 @@ def test_python_binding_refuses_cpu_tensors():
     ensure_built()
     with pytest.raises(ValueError):
         lrm.lrm_score(torch.zeros(4, 2), torch.zeros(4, 8), torch.zeros(4, 2, 8))
+
+
+def test_sizes_that_would_overflow_are_refused():
+    # T * k is never formed before T is known to keep it within int32 (no wrap-around to a
+    # small or negative pair count that would pass the later checks)
+    lib = ensure_built()
+    out = C.c_size_t(0)
+    assert lib.lrm_workspace_size(1 << 62, 8, 128, 2048, 768, 0, C.byref(out)) == 2
+    assert lib.lrm_workspace_size((1 << 31) // 8, 8, 128, 64, 64, 0, C.byref(out)) == 2   # P = 2^31
+    assert lib.lrm_workspace_size((1 << 31) // 8 - 1, 8, 8, 64, 64, 0, C.byref(out)) == 0
+    fn = lib.lrm_select_static
+    fn.restype = C.c_int
+    fn.argtypes = [C.c_void_p] * 3 + [C.c_int64, C.c_int32, C.c_int32, C.c_int64] + [C.c_void_p] * 5
+    fake = C.c_void_p(0x1000)
+    assert fn(fake, fake, fake, 1 << 62, 8, 16, 0, fake, fake, fake, None, None) == 2
+    assert fn(fake, fake, fake, (1 << 63) // 8, 8, 16, 0, fake, fake, fake, None, None) == 2

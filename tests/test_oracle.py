@@ -132,6 +132,35 @@ def autograd_pin_error(seed=0):
     return max(rel(out["dw_gate_up"], gWgu), rel(out["dw_down"], gWd), rel(out["dx"], gx))
 
 
+def recompute_autograd_pin_error(seed=0):
+    """quota = load on inputs without h and phi: the backward on the recomputed saved state against
+    torch fp64 autograd of the explicit forward."""
+    inp = fp64_consistent_inputs(seed)
+    T, k = inp["topk_idx"].shape
+    I = inp["w_down"].shape[2]
+    phi_sq = np.sum(inp["phi"] ** 2, axis=2)
+    lean = {n: v for n, v in inp.items() if n not in ("h", "phi")}
+    lean["phi_sq"] = phi_sq
+    loads = O.expert_loads(inp["topk_idx"], inp["w_down"].shape[0])
+    out = O.pruned_backward_recompute(lean, loads)
+    gWgu, gWd, gx, _ = explicit_forward_grads(inp)
+    return max(rel(out["dw_gate_up"], gWgu), rel(out["dw_down"], gWd), rel(out["dx"], gx))
+
+
+def recompute_matches_saved_state_error(seed=3):
+    """With the saved state exactly the fp64 forward of x, recomputing it changes nothing: the
+    pruned backward (quota below load) is the same either way."""
+    inp = fp64_consistent_inputs(seed, T=13, E=3, k=2)
+    E = inp["w_down"].shape[0]
+    _, q = O.plan_quotas(inp["topk_idx"], E, "ratio", 3, 5)
+    full = O.pruned_backward(inp, q)
+    lean = {n: v for n, v in inp.items() if n not in ("h", "phi")}
+    lean["phi_sq"] = np.sum(inp["phi"] ** 2, axis=2)
+    lean_out = O.pruned_backward_recompute(lean, q)
+    assert np.array_equal(full["kept_pair"], lean_out["kept_pair"])
+    return max(rel(lean_out[n], full[n]) for n in ("H_c", "Phi_c", "dw_gate_up", "dw_down", "dx"))
+
+
 def router_autograd_pin_error(seed=0):
     """quota = load: the oracle's dalpha against torch fp64 autograd's dL/dalpha."""
     inp = fp64_consistent_inputs(seed)
@@ -246,6 +275,15 @@ def test_swiglu_derivative_finite_differences():
 def test_full_quota_reduces_to_autograd_backward():
     for seed in range(3):
         assert autograd_pin_error(seed) < 1e-12
+
+
+def test_recomputed_state_full_quota_equals_autograd():
+    for seed in range(3):
+        assert recompute_autograd_pin_error(seed) < 1e-12
+
+
+def test_recomputed_state_equals_saved_state():
+    assert recompute_matches_saved_state_error() < 1e-12
 
 
 def test_router_grad_full_quota_equals_autograd():
@@ -434,6 +472,17 @@ def test_planted_mistakes_fail_a_pin(monkeypatch):
     with monkeypatch.context() as m:
         m.setattr(O, "scatter_dx", _planted_scatter_drops_last_choice)
         assert autograd_pin_error() > 1e-3
+    # recomputed saved state: gate and up rows of W_gate_up taken the wrong way round
+    real_recompute = O.recompute_saved_state
+
+    def recompute_swapped(kept_pair, topk_idx, x, w_gate_up, k):
+        W = np.asarray(w_gate_up)
+        I = W.shape[1] // 2
+        return real_recompute(kept_pair, topk_idx, x, np.concatenate([W[:, I:], W[:, :I]], axis=1), k)
+
+    with monkeypatch.context() as m:
+        m.setattr(O, "recompute_saved_state", recompute_swapped)
+        assert recompute_autograd_pin_error() > 1e-3
     # forward-side steps
     def route_ties_to_higher_id(L, k):
         idx, alpha = O.route(np.asarray(L)[:, ::-1], k)

@@ -64,6 +64,11 @@ WORKLOADS = {
     "qwen3_t32k_d30": Workload("qwen3_t32k_d30", 32768, 2048, 768, 128, 8, "bf16", 1.0, 1e-3, ("ratio", 7, 10)),
     # GLM4.5-106B-A12B-shaped routed-expert layer, drop 20 %
     "glm45_t32k_d20": Workload("glm45_t32k_d20", 32768, 4096, 1408, 128, 8, "bf16", 1.0, 1e-3, ("ratio", 8, 10)),
+    # a smaller case of the GLM4.5-shaped layer for counter captures that replay each kernel many
+    # times: the same H, I and k and the same mean retained rows per expert (8192 tokens over 32
+    # experts), about 5 GB on the device
+    "glm45_shape_t8k_e32": Workload("glm45_shape_t8k_e32", 8192, 4096, 1408, 32, 8, "bf16", 1.0, 1e-3,
+                                    ("ratio", 8, 10)),
     # overload stress: Zipf 1.5 skew, fixed row budget per expert
     "qwen3_t64k_zipf15_cap": Workload("qwen3_t64k_zipf15_cap", 65536, 2048, 768, 128, 8, "bf16", 1.5, 1e-3,
                                       ("cap", _cap(65536, 8, 128))),
