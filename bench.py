@@ -222,11 +222,18 @@ class OracleSample:
         q[sel] = self.quotas[sel]
         return q
 
-    def run(self, n=None):
+    def run(self, n=None, min_s=0.0):
+        """One oracle call on the first n experts of the order (repeated until min_s seconds have
+        passed, for samples that take milliseconds); returns (kept rows, seconds per call)."""
         n = self.n if n is None else n
-        t0 = time.perf_counter()
-        out = self.oracle.pruned_backward(self.npi, self.quotas_for(n))
-        return int(out["seg_offsets"][-1]), time.perf_counter() - t0
+        q = self.quotas_for(n)
+        reps, t0 = 0, time.perf_counter()
+        while True:
+            out = self.oracle.pruned_backward(self.npi, q)
+            reps += 1
+            dt = time.perf_counter() - t0
+            if dt >= min_s:
+                return int(out["seg_offsets"][-1]), dt / reps
 
     def calibrate(self, target_s, rounds=4):
         """Pick |S| so that one call takes about target_s.  The fixed cost comes from a call with no
@@ -252,28 +259,45 @@ class OracleSample:
 
     def describe(self):
         return (f"fp64 numpy oracle: score and selection of all {self.wl.P} pairs, backward of the "
-                f"{int(self.cum_rows[self.n])} retained rows of {self.n} of {self.wl.E} experts")
+                f"{int(self.cum_rows[self.n])} retained rows of {self.n} of {self.wl.E} experts, per call")
+
+
+_BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NVPL_BLAS_NUM_THREADS")
 
 
 def oracle_baseline(wl, inp, target_s=12.0, single_target_s=6.0):
-    """cpu_baseline of the bench line: the oracle on the host cores (all threads of its BLAS pool),
-    then the same on one thread, each on a sample sized to about its target time."""
-    from threadpoolctl import threadpool_limits
+    """cpu_baseline of the bench line: the oracle on the host cores (all threads of numpy's BLAS pool),
+    then, in a child process whose BLAS pool is held to one thread, the same on one thread; each on
+    a sample sized to about its target time."""
     smp = OracleSample(wl, oracle_inputs(inp))
     smp.calibrate(target_s)
-    R, dt = smp.run()
+    R, dt = smp.run(min_s=1.0)
     out = {"value": round(R / dt, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
            "sample": f"{smp.describe()} ({dt:.1f} s)"}
-    with threadpool_limits(1):
-        smp1 = OracleSample(wl, smp.npi)
-        smp1.calibrate(single_target_s)
-        R1, dt1 = smp1.run()
-    out["single_thread"] = {"value": round(R1 / dt1, 1), "unit": UNIT, "cores": 1,
-                            "sample": f"{smp1.describe()} ({dt1:.1f} s)"}
+    del smp
+    env = dict(os.environ, **{v: "1" for v in _BLAS_THREAD_VARS})
+    r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-single-thread", "--workload", wl.name,
+                        "--oracle-target-s", str(single_target_s)], env=env, capture_output=True, text=True)
+    try:
+        out["single_thread"] = json.loads(r.stdout.strip().splitlines()[-1])
+    except Exception:
+        out["single_thread"] = {"unavailable": (r.stderr.strip().splitlines() or ["no output"])[-1][:200]}
     return out
 
 
+def oracle_single_thread(wl, target_s):
+    """Child process of oracle_baseline (started with every BLAS pool held to one thread)."""
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    smp = OracleSample(wl, oracle_inputs(W.generate(wl, dev, seed=0)))
+    smp.calibrate(target_s)
+    R, dt = smp.run(min_s=1.0)
+    print(json.dumps({"value": round(R / dt, 1), "unit": UNIT, "cores": 1,
+                      "sample": f"{smp.describe()} ({dt:.1f} s)"}), flush=True)
+
+
 def cpu_threads():
+    """Threads of numpy's BLAS pool: threadpoolctl's answer where it is installed, else the thread
+    count the environment fixes, else every core (the BLAS libraries' default)."""
     try:
         from threadpoolctl import threadpool_info
         n = max((i.get("num_threads", 0) for i in threadpool_info()), default=0)
@@ -281,6 +305,9 @@ def cpu_threads():
             return n
     except Exception:
         pass
+    for v in _BLAS_THREAD_VARS:
+        if os.environ.get(v, "").isdigit():
+            return int(os.environ[v])
     return os.cpu_count()
 
 
@@ -294,6 +321,8 @@ def main():
     ap.add_argument("--workload", default="glm45_t32k_d20", choices=sorted(W.WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--simt", action="store_true", help="CUDA-core GEMMs instead of tcgen05 (comparison only)")
+    ap.add_argument("--oracle-single-thread", action="store_true", help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-target-s", type=float, default=6.0, help=argparse.SUPPRESS)
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the widened rows timed after the headline step (router gradient, compaction-free, "
                          "forward-side steps, ablation scores)")
@@ -305,6 +334,8 @@ def main():
     local = int(os.environ.get("LOCAL_RANK", "0"))
     wl = W.WORKLOADS[args.workload]
 
+    if args.oracle_single_thread:
+        return oracle_single_thread(wl, args.oracle_target_s)
     if args.impl == "reference":
         return reference_arm(args, wl, rank, world)
 
