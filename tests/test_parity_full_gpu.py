@@ -180,3 +180,69 @@ def test_full_size_compaction_free_bit_identical(name):
     for n in ("dw_gate_up", "dw_down", "dx"):
         assert torch.equal(getattr(a, n), getattr(b, n)), n
     assert torch.equal(a.dh_c[:R], b.dh_c[:R]) and torch.equal(a.dx_c[:R], b.dx_c[:R])
+
+
+@pytest.mark.parametrize("name", ["qwen3_t8k_d20", "glm45_t32k_d20"])
+def test_full_size_recompute(name):
+    """The variant whose forward kept x and ||phi_u||^2 only, at full size: selection bit-exact on its
+    own scores, recomputed h of sampled rows within one bf16 rounding (plus the fp32 sum bound) of the
+    oracle's, full per-expert dW of sampled experts and dX of sampled tokens against the oracle."""
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.WORKLOADS[name]
+    T, k, E, H, I = wl.T, wl.k, wl.E, wl.H, wl.I
+    tol = TOL[wl.dtype]
+    inp = W.generate(wl, "cuda", seed=0)
+    _, q = gpu_quotas(inp, wl)
+    _, phi_sq = lrm.lrm_swiglu_forward(inp["h"])
+    lean = {n: v for n, v in inp.items() if n not in ("h", "phi")}
+    lean["phi_sq"] = phi_sq
+    pb = lrm.PrunedBackward(T, k, E, H, I, dtype=wl.torch_dtype, compaction="recompute")
+    pb.run(lean, q)
+    torch.cuda.synchronize()
+    assert int(pb.dev_status.item()) == 0
+    del inp
+    cpu = {n: _np(v) for n, v in lean.items() if n not in ("w_gate_up", "w_down")}
+    idx = cpu["topk_idx"].astype(np.int64)
+    seg, kept, rop = oracle.select(idx, pb.scores.cpu().numpy(), to_np(q), E)
+    R = int(seg[-1])
+    assert np.array_equal(to_np(pb.seg_offsets), seg)
+    assert np.array_equal(to_np(pb.kept_pair)[:R], kept)
+
+    def weights(e):
+        return _np(lean["w_gate_up"][e])[None], _np(lean["w_down"][e])[None]
+
+    def expert_state(pairs, e):  # the oracle's compacted and recomputed rows of expert e's pairs
+        t = pairs // k
+        dY = cpu["alpha"].reshape(-1)[pairs].astype(np.float64)[:, None] * cpu["g"][t].astype(np.float64)
+        X = cpu["x"][t].astype(np.float64)
+        Hc, Phic = oracle.recompute_saved_state(np.arange(len(pairs)), np.zeros(len(pairs), np.int64), X,
+                                                weights(e)[0], 1)
+        return dY, X, Hc, Phic
+
+    rng = np.random.default_rng(2)
+    sizes = np.diff(seg)
+    nz = np.nonzero(sizes > 0)[0]
+    order = nz[np.argsort(sizes[nz], kind="stable")]
+    picks = sorted({int(order[-1]), int(order[len(order) // 2]), int(order[0])})
+    u = 2.0 ** -8
+    for e in picks:
+        pairs = kept[seg[e]:seg[e + 1]]
+        dY, X, Hc, Phic = expert_state(pairs, e)
+        r0 = int(seg[e])
+        assert rel_fro(_np(pb.h_c[r0:r0 + len(pairs)]).astype(np.float64), Hc) <= u + TOL["f32"], (name, e, "h_c")
+        dWgu, dWd, dH, dXc = oracle.expert_backward(np.array([0, len(pairs)]), dY, X, Hc, Phic, *weights(e))
+        assert rel_fro(_np(pb.dw_down[e]), dWd[0]) <= tol, (name, e, "dw_down")
+        assert rel_fro(_np(pb.dw_gate_up[e]), dWgu[0]) <= tol, (name, e, "dw_gate_up")
+    toks = np.sort(rng.choice(T, size=min(T, 128), replace=False))
+    pairs = np.array([v for t in toks for v in range(t * k, t * k + k) if rop[v] >= 0], dtype=np.int64)
+    pe = idx.reshape(-1)[pairs]
+    dXc = np.zeros((len(pairs), H))
+    for e in np.unique(pe):
+        sel = np.nonzero(pe == e)[0]
+        dY, X, Hc, Phic = expert_state(pairs[sel], int(e))
+        dXc[sel] = oracle.expert_backward(np.array([0, len(sel)]), dY, X, Hc, Phic, *weights(int(e)))[3]
+    sub_rop = np.full(T * k, -1, np.int64)
+    sub_rop[pairs] = np.arange(len(pairs))
+    want = oracle.scatter_dx(sub_rop, dXc, T, k)[toks]
+    got = _np(pb.dx.index_select(0, torch.as_tensor(toks, device="cuda"))).astype(np.float64)
+    assert rel_fro(got, want) <= tol, (name, "dx", rel_fro(got, want))

@@ -63,6 +63,31 @@ def test_static_select_matches_workspace_select_twice(lib):
             assert torch.equal(a, b)  # selection is integer work: bit-exact
 
 
+def test_static_select_matches_the_oracle(lib):
+    # the same selection, checked against the oracle's top-quota rule on the GPU's own fp32 scores
+    import oracle
+    import pruned_expert_backward_gb300 as lrm
+    wl = W.small_workload("na3", 2500, 256, 128, 32, 8)
+    inp = W.generate(wl, "cuda", seed=3)
+    _, q = lrm.lrm_plan_quotas(inp["topk_idx"], wl.E, "ratio", 8, 10)
+    scores = lrm.lrm_score(inp["alpha"], inp["g"], inp["phi"])
+    P = wl.T * wl.k
+    seg = torch.empty(wl.E + 1, dtype=torch.int32, device="cuda")
+    kept = torch.empty(P, dtype=torch.int32, device="cuda")
+    rop = torch.empty(P, dtype=torch.int32, device="cuda")
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    rc = lib.lrm_select_static(inp["topk_idx"].data_ptr(), scores.data_ptr(), q.data_ptr(), wl.T, wl.k, wl.E, P,
+                               seg.data_ptr(), kept.data_ptr(), rop.data_ptr(), st.data_ptr(),
+                               torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert rc == 0 and int(st.item()) == 0
+    oseg, okept, orop = oracle.select(inp["topk_idx"].cpu().numpy(), scores.cpu().numpy(), q.cpu().numpy(), wl.E)
+    R = int(oseg[-1])
+    assert np.array_equal(seg.cpu().numpy(), oseg)
+    assert np.array_equal(kept[:R].cpu().numpy(), okept)
+    assert np.array_equal(rop.cpu().numpy(), orop)
+
+
 def test_static_select_rejects_sizes_beyond_its_array(lib):
     dummy = torch.zeros(16, dtype=torch.int32, device="cuda")
     p = dummy.data_ptr()
