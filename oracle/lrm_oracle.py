@@ -371,7 +371,9 @@ def pruned_backward_recompute(inp, quotas, scores=None):
     """The pruned backward of a forward that kept x and phi_sq = ||phi_u||^2 instead of h and phi:
     score from the norms, select, compact dY_c and X_c, recompute H_c and Phi_c for the kept rows,
     then the grouped backward and the return to token order.  inp holds topk_idx, alpha, x, g,
-    phi_sq [T,k], w_gate_up, w_down.  `scores` overrides the selection scores as in pruned_backward."""
+    phi_sq [T,k], w_gate_up, w_down.  `scores` overrides the selection scores as in pruned_backward.
+    Pinned: with quota = load it equals torch fp64 autograd of the explicit forward; on inputs whose
+    h and phi are the exact fp64 forward of x it equals pruned_backward (tests/test_oracle.py)."""
     idx = _np(inp["topk_idx"])
     T, k = idx.shape
     E = _np(inp["w_down"]).shape[0]

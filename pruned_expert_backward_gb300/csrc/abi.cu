@@ -44,7 +44,7 @@ bool nvtx_enabled() {
 void nvtx_push(const char* name) { nvtxRangePushA(name); }
 void nvtx_pop() { nvtxRangePop(); }
 
-size_t gemm_plan_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 2)); }
+size_t gemm_plan_bytes(int32_t E) { return up(sizeof(int32_t) * (2 * (size_t)E + 3 + kTileCounters)); }
 size_t gemm_ws_bytes(int32_t E) { return gemm_plan_bytes(E) + 128 * 6 * (size_t)E; }
 
 // lrm_grouped_backward's scratch: tile tables and tensor maps, then (only when row_dot is

@@ -133,6 +133,9 @@ struct TcParams {
   // (dh_c viewed as [rows][2][I], dx_c as [rows][H]), and tmC the gate/up map of h_c ([rows][2][I]).
   int tma_epi;
   int gP;  // gather mode: pairs in h / phi (T*k); a kept_pair entry outside [0, gP) is not followed
+  // var-K launches: counter of the dynamic tile order (see TileSeq), used when the plan kernel
+  // switched it on for this call (plan[2E+2] = 1)
+  int32_t* tile_counter;
 };
 
 // Pair named by kept_pair for a gathered row: in [0, gP), or -1 (flagged; the row reads as zeros).
@@ -417,13 +420,78 @@ template <int S>
 __host__ __device__ constexpr uint32_t epi_offset() { return (uint32_t)S * kStageBytes; }
 template <int S>
 __host__ __device__ constexpr uint32_t bar_offset() { return epi_offset<S>() + kEpiWarps * epi_bytes<S>(); }
-// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, gathered[S], then two per epilogue
-// warp for its gate/up buffers
+// Tile ring of the dynamic tile order: the leader's producer publishes each tile index it takes
+// into kRing slots in both CTAs; every other role of the pair reads it there and frees the slot on
+// the leader's tile_empty barrier (kRingReaders arrivals: the MMA issuer, the other CTA's producer
+// and the epilogue warps of both CTAs).
+constexpr int kRing = 16;
+constexpr int kRingReaders = 2 + 2 * kEpiWarps;
+// barriers: full[S], empty[S], acc_full[2], acc_empty[2], drain, gathered[S], two per epilogue
+// warp for its gate/up buffers, then tile_full[kRing], tile_empty[kRing]
 template <int S>
-__host__ __device__ constexpr int n_barriers() { return 3 * S + 5 + 2 * kEpiWarps; }
+__host__ __device__ constexpr int n_barriers() { return 3 * S + 5 + 2 * kEpiWarps + 2 * kRing; }
+template <int S>
+__host__ __device__ constexpr int ring_bar_index() { return 3 * S + 5 + 2 * kEpiWarps; }
+
+// The tile sequence of one role of a CTA pair.  Static order: pair, pair + n_pairs, ...  Dynamic
+// order (var-K launches with long tiles): the leader's producer takes tiles from a global counter
+// in plan order as its pair becomes free and publishes them (take / publish), one tile ahead of its
+// own loads; the other roles read them from their CTA's ring (next).  The tiles running at any moment
+// are then consecutive in the plan whatever their lengths, so the tiles of one expert stay together
+// in time and share its operand rows through L2; with the fixed round robin the pairs drift apart
+// once experts of different lengths mix, and an expert's rows are fetched from DRAM again and again.
+// A value >= n_tiles ends the sequence; -1 means a wait gave up.
+struct TileSeq {
+  bool dyn;
+  int t, n_tiles, n_pairs;
+  uint32_t full0, empty0, empty_lead;  // this CTA's tile_full / tile_empty, the leader's tile_empty
+  volatile int* slots;                 // this CTA's ring
+  uint32_t slot, ph;
+  volatile int* abort;
+  int32_t* status;
+  bool local;  // a reader in the leader CTA (releases its slot on its own CTA's barrier)
+
+  __device__ __forceinline__ int first(int pair) {
+    if (!dyn) return t = pair;
+    return t = read();
+  }
+  __device__ __forceinline__ int next() {
+    if (!dyn) return t += n_pairs;
+    return t = read();
+  }
+  // reader side (one thread)
+  __device__ __forceinline__ int read() {
+    if (!mbar_wait_cl(full0 + 8 * slot, ph, abort, status)) return -1;
+    const int v = slots[slot];
+    if (local)
+      asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(empty0 + 8 * slot) : "memory");
+    else
+      mbar_arrive_release_cluster(empty_lead + 8 * slot);
+    if (++slot == (uint32_t)kRing) { slot = 0; ph ^= 1u; }
+    return v;
+  }
+  // taker side (the leader's producer thread)
+  __device__ __forceinline__ int take(int32_t* counter) {
+    const int v = atomicAdd(counter, 1);
+    return v < n_tiles ? v : n_tiles;
+  }
+  __device__ __forceinline__ bool publish(int v, uint32_t remote_slots, uint32_t remote_full0) {
+    if (!mbar_wait_cl(empty0 + 8 * slot, ph ^ 1u, abort, status)) return false;  // all readers freed it
+    slots[slot] = v;
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(remote_slots + 4 * slot), "r"(v) : "memory");
+    mbar_arrive_release_cluster(cluster_addr(full0 + 8 * slot, 0));
+    mbar_arrive_release_cluster(remote_full0 + 8 * slot);
+    if (++slot == (uint32_t)kRing) { slot = 0; ph ^= 1u; }
+    t = v;
+    return true;
+  }
+};
+
 
 // ---------------------------------------------------------------- the kernel ---------
-template <int S>
+// S: operand pipeline depth.  RING: the kernel can follow the dynamic tile order (the var-K
+// launches); the others are compiled without it.
+template <int S, bool RING>
 __global__ void __launch_bounds__(kThreads, 1)
     tc_grouped_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                       const __grid_constant__ CUtensorMap tmC, const TcParams p) {
@@ -433,6 +501,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + bar_offset<S>());
   uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(bars + n_barriers<S>());
   int* abort_flag = reinterpret_cast<int*>(tmem_holder + 1);
+  int* ring_slots = abort_flag + 1;  // [kRing]
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rank = (int)cluster_rank();
@@ -458,6 +527,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(acce0 + 8, 2 * kEpiWarps);
     mbar_init(drain, 1);
     for (int i = 0; i < 2 * kEpiWarps; ++i) mbar_init(smem_u32(bars + 3 * S + 5 + i), 1);
+    for (int i = 0; i < kRing; ++i) {
+      mbar_init(smem_u32(bars + ring_bar_index<S>() + i), 1);                     // tile_full: the taker
+      mbar_init(smem_u32(bars + ring_bar_index<S>() + kRing + i), kRingReaders);  // tile_empty (leader's)
+    }
     *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -472,6 +545,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int n_tiles = total_tiles(p);
   volatile int* abortv = abort_flag;
   const uint32_t full_lead = cluster_addr(full0, 0), acce_lead = cluster_addr(acce0, 0);
+  const uint32_t tfull0 = smem_u32(bars + ring_bar_index<S>()), tempty0 = tfull0 + 8 * kRing;
+  // this role's tile sequence (TileSeq): dynamic for the var-K launches when the plan kernel chose it
+  const bool dyn_order =
+      RING && p.kind == VK && p.tile_counter != nullptr && !gather_b && __ldg(p.plan + 2 * p.E + 2) == 1;
+  TileSeq seq{dyn_order, 0, n_tiles, n_pairs, tfull0, tempty0, cluster_addr(tempty0, 0), ring_slots, 0u, 0u,
+              abort_flag, p.status, leader};
 
   const int first_extra = 2 + kEpiWarps;  // warps first_extra.. are the extra gather warps
   if (gather_b && (warp == 0 || warp >= first_extra)) {
@@ -580,7 +659,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t it = 0, st = 0, sph = 0;  // iteration count, its stage and phase
       bool ok = true;
       int last_e = -1;
-      for (int t = pair; t < n_tiles && ok; t += n_pairs) {
+      // dynamic order: the leader's producer is the taker and publishes into both CTAs' rings
+      const bool taker = seq.dyn && leader;
+      const uint32_t rslots = cluster_addr(smem_u32(ring_slots), 1), rfull0 = cluster_addr(tfull0, 1);
+      // The taker keeps the ring one tile ahead of its own loads: when it starts tile t, tile t's
+      // successor is already published, and the tile after that is taken from the counter (the
+      // atomic's round trip overlaps t's loads) and published once t's loads are queued.
+      int t, t_next = n_tiles;
+      if (taker) {
+        t = seq.take(p.tile_counter);
+        if (!seq.publish(t, rslots, rfull0)) t = -1;
+        if (t >= 0 && t < n_tiles) {
+          t_next = seq.take(p.tile_counter);
+          if (!seq.publish(t_next, rslots, rfull0)) t = -1;
+        }
+      } else {
+        t = seq.first(pair);
+      }
+      while (t >= 0 && t < n_tiles && ok) {
+        const int t_after = taker && t_next < n_tiles ? seq.take(p.tile_counter) : n_tiles;
         const Tile d = decode(p, t, rank);
         const CUtensorMap* ma = &tmA;
         const CUtensorMap* mb = &tmB;
@@ -632,6 +729,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
         }
+        if (!ok) break;
+        if (taker) {
+          if (t_next < n_tiles && !seq.publish(t_after, rslots, rfull0)) break;
+          t = t_next;
+          t_next = t_after;
+        } else {
+          t = seq.next();
+        }
       }
       // drain: every stage this thread filled has been consumed (so its data landed)
       const uint32_t first = it > (uint32_t)S ? it - S : 0u;
@@ -657,7 +762,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t st = 0, sph = 0;
         int lt = 0;
         bool ok = true;
-        for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+        // the next tile is read before this one's MMAs are issued (it is published a tile ahead), so
+        // no ring access sits between two tiles' MMAs
+        int t = seq.first(pair);
+        for (int tn; t >= 0 && t < n_tiles && ok; t = tn, ++lt) {
+          tn = seq.next();
           const Tile d = decode(p, t, 0);
           const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
           if (!mbar_wait(acce0 + 8 * acc, acc_ph ^ 1u, abortv, p.status)) break;
@@ -734,7 +843,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_e = -1;
     bool ok = true;
     int lt = 0;
-    for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+    auto tile_at = [&](bool first) {  // lane 0 follows the pair's tile sequence for the warp
+      int v = 0;
+      if (lane == 0) v = first ? seq.first(pair) : seq.next();
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    for (int t = tile_at(true); t >= 0 && t < n_tiles && ok; t = tile_at(false), ++lt) {
       const Tile d = decode(p, t, rank);
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
       const int row_base = d.row0 + q * 32;
@@ -812,7 +926,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     int last_e = -1;
     bool ok = true;
     int lt = 0;
-    for (int t = pair; t < n_tiles && ok; t += n_pairs, ++lt) {
+    auto tile_at = [&](bool first) {  // lane 0 follows the pair's tile sequence for the warp
+      int v = 0;
+      if (lane == 0) v = first ? seq.first(pair) : seq.next();
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    for (int t = tile_at(true); t >= 0 && t < n_tiles && ok; t = tile_at(false), ++lt) {
       const Tile d = decode(p, t, rank);
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
       const int row_base = d.row0 + q * 32;
@@ -937,7 +1056,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int sub = lane >> 2, piece = lane & 3;  // var-M stores: lane owns 8 columns of one row
     float* stg = reinterpret_cast<float*>(epi + ew * (p.kind == VK ? kBoxBytes : epi_bytes<S>()));
     int lt = 0;
-    for (int t = pair; t < n_tiles; t += n_pairs, ++lt) {
+    auto tile_at = [&](bool first) {  // lane 0 follows the pair's tile sequence for the warp
+      int v = 0;
+      if (lane == 0) v = first ? seq.first(pair) : seq.next();
+      return __shfl_sync(0xffffffffu, v, 0);
+    };
+    for (int t = tile_at(true); t >= 0 && t < n_tiles; t = tile_at(false), ++lt) {
       const Tile d = decode(p, t, rank);
       const uint32_t acc = lt & 1, acc_ph = (lt >> 1) & 1;
       const int row_base = p.kind == VK ? d.m0 + q * 32 : d.row0 + q * 32;
@@ -1083,6 +1207,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Tile tables from seg_offsets: plan[0..E] = exclusive prefix of ceil(R_e / 256) (var-M pair tiles),
 // plan[E+1 .. 2E] = experts ordered by R_e descending, ties by expert id (var-K, longest first),
+// plan[2E+2] = 1 for the dynamic tile order of the var-K launches (mean rows per expert at least
+// kDynMinRowsPerExpert), plan[2E+3 ..] = their tile counters (zeroed here),
 // plan[2E+1] = 1 if seg_offsets is a segmentation of [0, seg_offsets[E]] within [0, cap]
 // (seg_offsets[0] = 0, no decreasing step, seg_offsets[E] <= cap), else 0: then
 // LRM_ERR_BAD_SEGMENTS is recorded and the GEMM launches run no tile (total_tiles), so no map
@@ -1091,6 +1217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Templates 0-3: var-K operands (row extent is dimension 1); 4: dh_c as [rows][2][I] (rows are
 // dimension 2); 5: dx_c as [rows][H] (dimension 1).
 constexpr int kMapSets = 6;
+constexpr int kDynMinRowsPerExpert = 1024;
 struct MapTemplates {
   CUtensorMap t[kMapSets];
 };
@@ -1110,7 +1237,11 @@ __global__ void __launch_bounds__(1024) tc_plan_kernel(const int32_t* __restrict
   if (e == 0) {
     plan[2 * E + 1] = valid ? 1 : 0;
     if (!valid) set_status(status, LRM_ERR_BAD_SEGMENTS);
+    // dynamic tile order for the var-K launches when their tiles are long (TileSeq): below this
+    // mean the ring's round trip per tile costs more than the L2 reuse it buys
+    plan[2 * E + 2] = valid && (int64_t)seg[E] >= (int64_t)kDynMinRowsPerExpert * E ? 1 : 0;
   }
+  if (e < kTileCounters) plan[2 * E + 3 + e] = 0;  // the var-K launches' tile counters
   const int r = e < E && valid ? seg[e + 1] - seg[e] : 0;
   if (e < E) s_r[e] = r;
   const int mt = (r + 2 * kBM - 1) / (2 * kBM);
@@ -1292,7 +1423,7 @@ bool make_map_out3d(CUtensorMap* m, void* base, uint64_t E, uint64_t M, uint64_t
 }
 
 template <int S>
-size_t smem_bytes() { return 1024 + bar_offset<S>() + n_barriers<S>() * 8 + 8; }
+size_t smem_bytes() { return 1024 + bar_offset<S>() + n_barriers<S>() * 8 + 8 + 4 * kRing; }
 
 int sm_count() {
   static int count[kDeviceSlots] = {};
@@ -1316,11 +1447,11 @@ bool device_ok() {
   return major == 10 && minor == 3;
 }
 
-template <int S>
+template <int S, bool RING>
 lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUtensorMap& c, const TcParams& p,
                          int64_t tiles_bound, cudaStream_t s) {
   const size_t smem = smem_bytes<S>();
-  if (ensure_max_smem<tc_grouped_kernel<S>>((int)smem) != cudaSuccess) return LRM_ERR_CUDA;
+  if (ensure_max_smem<tc_grouped_kernel<S, RING>>((int)smem) != cudaSuccess) return LRM_ERR_CUDA;
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[2];
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see chain_wait()
@@ -1341,14 +1472,14 @@ lrm_status launch_stages(const CUtensorMap& a, const CUtensorMap& b, const CUten
   if (max_pairs == 0) {
     cfg.gridDim = dim3(2 * sm_count() / 2);
     int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_kernel<S>, &cfg) != cudaSuccess || n <= 0) n = sm_count() / 2;
+    if (cudaOccupancyMaxActiveClusters(&n, tc_grouped_kernel<S, RING>, &cfg) != cudaSuccess || n <= 0) n = sm_count() / 2;
     max_pairs = n;
     if (dslot >= 0) max_pairs_dev[dslot] = n;
   }
   cfg.numAttrs = 2;
   const int64_t pairs = tiles_bound < max_pairs ? tiles_bound : max_pairs;
   cfg.gridDim = dim3((unsigned)(2 * pairs));
-  if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel<S>, a, b, c, p) != cudaSuccess) return LRM_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, tc_grouped_kernel<S, RING>, a, b, c, p) != cudaSuccess) return LRM_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? LRM_OK : LRM_ERR_CUDA;
 }
 
@@ -1356,8 +1487,9 @@ lrm_status launch_one(const CUtensorMap& a, const CUtensorMap& b, const CUtensor
                       int64_t tiles_bound, cudaStream_t s) {
   if (tiles_bound <= 0) return LRM_OK;
   // dphi + SwiGLU and the recomputed forward state need the wide per-warp epilogue buffers
-  return p.kind == VM_SWIGLU || p.kind == VM_FWD ? launch_stages<kSwigluStages>(a, b, c, p, tiles_bound, s)
-                                                 : launch_stages<kStages>(a, b, c, p, tiles_bound, s);
+  if (p.kind == VK) return launch_stages<kStages, true>(a, b, c, p, tiles_bound, s);
+  return p.kind == VM_SWIGLU || p.kind == VM_FWD ? launch_stages<kSwigluStages, false>(a, b, c, p, tiles_bound, s)
+                                                 : launch_stages<kStages, false>(a, b, c, p, tiles_bound, s);
 }
 
 }  // namespace
@@ -1444,6 +1576,8 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   mB = tpl.t[1];
   CUtensorMap mC;
   if (!make_map_out3d(&mC, g.dw_down, E, H, I)) return LRM_ERR_CUDA;
+  int32_t* counters = plan + 2 * E + 3;  // zeroed by the plan kernel
+  p.tile_counter = counters + 0;
   if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dW_gate_up[e] = dh_c^T x_c  (M = 2I, N = H)
   p = TcParams{VK, E, 2 * I, H, 0, (2 * I + kBM - 1) / kBM, (H + kBN - 1) / kBN, g.seg_offsets, plan,
@@ -1452,6 +1586,7 @@ lrm_status launch_grouped_tc(const GroupedArgs& g, const GemmWs& ws, cudaStream_
   mA = tpl.t[2];
   mB = tpl.t[3];
   if (!make_map_out3d(&mC, g.dw_gate_up, E, 2 * I, H)) return LRM_ERR_CUDA;
+  p.tile_counter = counters + 1;
   if ((st = launch_one(mA, mB, mC, p, (int64_t)E * ((p.nM + 1) / 2) * p.nN, s))) return st;
   // dx_c = dh_c W_gate_up[e]  (K = 2I, N = H)
   if (!make_map_2d(&mA, g.dh_c, rows, 2 * I, kBM) || !vm_map(&mB, g.w_gate_up, 2 * I, H, &vm_merged))

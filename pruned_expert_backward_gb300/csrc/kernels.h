@@ -26,10 +26,12 @@ struct SelectWs {
 // Scratch of the tensor-core grouped GEMMs: tile tables, then 6*E per-expert TMA tensor maps
 // (128 bytes each, 128-byte aligned) built on the device from seg_offsets.
 struct GemmWs {
-  int32_t* plan;  // [2E+2]
+  int32_t* plan;  // [2E+3+kTileCounters]
   void* maps;     // [6][E] CUtensorMap
 };
-size_t gemm_plan_bytes(int32_t E);  // plan[2E+2]: tile tables and the segment-check word
+// var-K launches of one grouped call whose tile counters sit in the plan region
+constexpr int kTileCounters = 2;
+size_t gemm_plan_bytes(int32_t E);  // plan[2E+3+kTileCounters]: tile tables, checks, tile counters
 size_t gemm_ws_bytes(int32_t E);
 
 struct WsLayout {
