@@ -104,3 +104,23 @@ def test_sizes_that_would_overflow_are_refused():
     fake = C.c_void_p(0x1000)
     assert fn(fake, fake, fake, 1 << 62, 8, 16, 0, fake, fake, fake, None, None) == 2
     assert fn(fake, fake, fake, (1 << 63) // 8, 8, 16, 0, fake, fake, fake, None, None) == 2
+
+
+def test_recompute_forward_host_validation():
+    lib = ensure_built()
+    fn = lib.lrm_recompute_forward
+    fake = C.c_void_p(0x1000)
+    ws = C.c_size_t(0)
+    assert lib.lrm_workspace_size(0, 1, 8, 64, 32, 0, C.byref(ws)) == 0
+    # null seg_offsets / weights; null row buffers with rows to hold
+    assert fn(None, fake, fake, 8, 64, 32, 0, 16, fake, fake, fake, ws.value, 0, None, None) == 1
+    assert fn(fake, fake, None, 8, 64, 32, 0, 16, fake, fake, fake, ws.value, 0, None, None) == 1
+    assert fn(fake, None, fake, 8, 64, 32, 0, 16, fake, fake, fake, ws.value, 0, None, None) == 1
+    # unknown flag, bad dtype, sizes outside the limits, misaligned pointer, workspace too small
+    assert fn(fake, fake, fake, 8, 64, 32, 0, 16, fake, fake, fake, ws.value, 7, None, None) == 1
+    assert fn(fake, fake, fake, 8, 64, 32, 9, 16, fake, fake, fake, ws.value, 0, None, None) == 3
+    assert fn(fake, fake, fake, 8, 60, 32, 0, 16, fake, fake, fake, ws.value, 0, None, None) == 2
+    assert fn(fake, C.c_void_p(0x1008), fake, 8, 64, 32, 0, 16, fake, fake, fake, ws.value, 0, None, None) == 1
+    assert fn(fake, fake, fake, 8, 64, 32, 0, 16, fake, fake, fake, 16, 0, None, None) == 4
+    # nothing to recompute (cap = 0): accepted, nothing launched
+    assert fn(fake, None, fake, 8, 64, 32, 0, 0, None, None, fake, ws.value, 0, None, None) == 0
