@@ -180,12 +180,14 @@ def oracle_inputs(inp):
 
 
 class OracleSample:
-    """The fp64 oracle on a bounded sample of a workload: every token and every pair is scored and
-    selected, and the backward runs on the retained rows of a subset S of the experts (the other
-    experts' quotas are set to 0, so the oracle computes nothing for them).  An expert's backward
-    depends on its own rows only, so a kept row costs the oracle what it costs in the whole
-    workload.  S takes experts in proportion to the retained rows they hold (see __init__) until
-    one call takes about the target time."""
+    """The fp64 oracle on a bounded sample of a workload: a subset S of the experts.  One call runs
+    the whole oracle (score, selection, compaction, expert backward, return to token order) on the
+    tokens routed to an expert of S, with the quotas of the other experts set to 0.  An expert's
+    selection and backward depend on its own pairs and rows only, so every retained row of S costs
+    the oracle what it costs in the whole workload; the tokens' other pairs are scored too.  S takes
+    experts in proportion to the retained rows they hold (see __init__) until one call takes about
+    the target time; when one expert alone takes longer, its quota is cut to the rows that fit (its
+    top rows by score: the same work per row)."""
 
     def __init__(self, wl, npi):
         import oracle
@@ -213,53 +215,88 @@ class OracleSample:
         order += [e for e in range(wl.E) if e not in seen and kept[e] > 0]
         order += [e for e in range(wl.E) if kept[e] == 0]
         self.order = order
+        self.kept = kept
         self.cum_rows = np.concatenate([[0], np.cumsum(kept[self.order])])
-        self.n = wl.E
+        self.n, self.frac = wl.E, 1.0
+        self._sub = {}
 
-    def quotas_for(self, n):
+    def quotas_for(self, n, frac=1.0):
         q = np.zeros_like(self.quotas)
         sel = self.order[:n]
         q[sel] = self.quotas[sel]
+        if frac < 1.0 and n == 1:
+            e = sel[0]
+            q[e] = max(1, int(min(self.quotas[e], self.loads[e]) * frac))
         return q
 
-    def run(self, n=None, min_s=0.0):
+    def inputs_for(self, n):
+        """The tokens with a pair routed to one of the first n experts of the order (input
+        preparation, outside the timed call)."""
+        if n not in self._sub:
+            idx = np.asarray(self.npi["topk_idx"])
+            tok = np.nonzero(np.isin(idx, np.asarray(self.order[:n], dtype=idx.dtype)).any(axis=1))[0]
+            sub = {}
+            for name, v in self.npi.items():
+                sub[name] = v if name in ("w_gate_up", "w_down") else np.ascontiguousarray(v[tok])
+            self._sub = {n: (sub, int(tok.shape[0]))}
+        return self._sub[n]
+
+    def rows(self, n=None, frac=None):
+        n = self.n if n is None else n
+        frac = self.frac if frac is None else frac
+        return int(np.minimum(np.maximum(self.quotas_for(n, frac), 0), self.loads).sum())
+
+    def run(self, n=None, min_s=0.0, frac=None):
         """One oracle call on the first n experts of the order (repeated until min_s seconds have
         passed, for samples that take milliseconds); returns (kept rows, seconds per call)."""
         n = self.n if n is None else n
-        q = self.quotas_for(n)
+        frac = self.frac if frac is None else frac
+        q = self.quotas_for(n, frac)
+        sub, _ = self.inputs_for(n)
         reps, t0 = 0, time.perf_counter()
         while True:
-            out = self.oracle.pruned_backward(self.npi, q)
+            out = self.oracle.pruned_backward(sub, q)
             reps += 1
             dt = time.perf_counter() - t0
             if dt >= min_s:
                 return int(out["seg_offsets"][-1]), dt / reps
 
     def calibrate(self, target_s, rounds=4):
-        """Pick |S| so that one call takes about target_s.  The fixed cost comes from a call with no
-        expert; the per-row cost from the latest measured call, refined over a few calls (the cost
-        of a row depends on its expert's size)."""
-        _, f = self.run(0)
-        n = 1
-        r, t = self.run(n)
+        """Pick |S| (and, for one expert, the share of its rows) so that one call takes about
+        target_s, from the measured cost per retained row, refined over a few calls (the cost of a
+        row depends on its expert's size and on the tokens that come with it)."""
+        def timed(n, frac=1.0):  # the faster of two calls: host timings are noisy
+            r, t = self.run(n, frac=frac)
+            return r, min(t, self.run(n, frac=frac)[1])
+
+        n, frac = 1, 1.0
+        self.run(n, frac=frac)  # warm-up: the first call also pays for thread start and page faults
+        r, t = timed(n)
         for _ in range(rounds):
-            c = max(t - f, 1e-6) / max(r, 1)
+            if t > 1.5 * target_s and n == 1:
+                frac = max(frac * target_s / t, 1.0 / max(1, int(self.kept[self.order[0]])))
+                r, t = timed(1, frac)
+                continue
+            c = t / max(r, 1)
             m = 1
-            while m < self.wl.E and f + c * self.cum_rows[m + 1] <= target_s:
+            while m < self.wl.E and c * self.cum_rows[m + 1] <= target_s:
                 m += 1
-            if m == n:
+            if m == n or frac < 1.0:
                 break
             n = m
-            r, t = self.run(n)
+            r, t = timed(n)
             if t > 1.5 * target_s and n > 1:
                 n = max(1, n // 2)
-                r, t = self.run(n)
-        self.n = n
+                r, t = timed(n)
+        self.n, self.frac = n, frac
         return n
 
     def describe(self):
-        return (f"fp64 numpy oracle: score and selection of all {self.wl.P} pairs, backward of the "
-                f"{int(self.cum_rows[self.n])} retained rows of {self.n} of {self.wl.E} experts, per call")
+        _, ntok = self.inputs_for(self.n)
+        share = "" if self.frac >= 1.0 else f" (its top {self.frac:.0%} by score)"
+        return (f"fp64 numpy oracle on the {ntok} of {self.wl.T} tokens routed to {self.n} of {self.wl.E} "
+                f"experts: score and selection of their {ntok * self.wl.k} pairs, backward of the "
+                f"{self.rows()} retained rows of those experts{share}, per call")
 
 
 _BLAS_THREAD_VARS = ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS", "NVPL_BLAS_NUM_THREADS")
@@ -649,7 +686,8 @@ def end_to_end(args, wl, inp, quotas, pb, step, stream, R_total, pg, dev):
 
 def reference_arm(args, wl, rank, world):
     """fp64 CPU oracle on the host cores: each step is one oracle call on a bounded sample of the
-    workload (OracleSample; the sample is sized during the warm-up steps to about 4 s per call)."""
+    workload (OracleSample; the sample is sized before the warm-up steps to about 4 s per call, or
+    to 150 s over all steps when that is less)."""
     if rank != 0:
         return
     # inputs drawn with the same generator, on the GPU where there is one (drawing the largest
@@ -658,7 +696,8 @@ def reference_arm(args, wl, rank, world):
     inp = W.generate(wl, dev, seed=0)
     smp = OracleSample(wl, oracle_inputs(inp))
     del inp
-    smp.calibrate(4.0)
+    # per call about 4 s, less when many steps are asked for, so that the run ends in a few minutes
+    smp.calibrate(min(4.0, max(0.25, 150.0 / max(1, args.steps + args.warmup))))
     for _ in range(max(0, args.warmup - 2)):
         smp.run()
     t0 = time.perf_counter()
@@ -672,7 +711,7 @@ def reference_arm(args, wl, rank, world):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {"workload": wl.name, "T": wl.T, "H": wl.H, "I": wl.I, "E": wl.E, "k": wl.k,
-                   "quota": quota_text(wl), "sample_experts": smp.n, "sample_rows": int(smp.cum_rows[smp.n])},
+                   "quota": quota_text(wl), "sample_experts": smp.n, "sample_rows": smp.rows()},
         "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cpu_threads(), "kind": "oracle",
                          "sample": smp.describe()},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

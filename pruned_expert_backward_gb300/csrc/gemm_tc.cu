@@ -31,6 +31,9 @@
 // them out through TMA stores.  Two 256-column fp32 accumulators in TMEM let the epilogue of
 // one tile overlap the MMAs of the next; both CTAs' epilogues release an accumulator on the
 // leader's barrier.
+// Tiles go to the CTA pairs round robin, except in the var-K launches of a call with long tiles
+// (mean retained rows per expert >= kDynMinRowsPerExpert, decided on the device by the plan
+// kernel), where each pair takes its next tile from a global counter as it becomes free (TileSeq).
 //
 // Shared-memory operand layouts are the 128-byte-swizzled canonical forms:
 //   K-major  (rows of 64 K-elements = 128 B): SBO = 1024 B between 8-row groups;
