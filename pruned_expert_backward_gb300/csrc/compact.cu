@@ -11,7 +11,7 @@
 // scaled by alpha_u) into each kept pair's row; the token's k rows of h and phi are one
 // contiguous span, read only where the pair is kept.  16-byte coalesced loads and stores.
 //
-// scatter_dx: a CTA covers 16 tokens; each thread owns one 16-byte column slice, walks the
+// scatter_dx: a CTA covers 8 tokens; each thread owns one 16-byte column slice, walks the
 // CTA's kept rows with 8 loads in flight and adds each token's rows in j order in fp32
 // (deterministic, no atomics).
 #include "common.cuh"
@@ -93,7 +93,7 @@ __global__ void __launch_bounds__(256) compact_kernel(const int32_t* __restrict_
 // in shared memory; then every thread walks that list for one 16-byte column slice, keeping
 // kScatterLoads row loads in flight however few rows each token kept, and adds each token's rows
 // in j order in fp32 (deterministic: the same sum in the same order as one row at a time).
-constexpr int kScatterTok = 16;
+constexpr int kScatterTok = 8;  // 16: 5 % slower at T = 32768 (fewer CTAs, longer lists), 32: slower still
 constexpr int kScatterLoads = 8;
 
 template <typename T>
