@@ -459,6 +459,7 @@ def main():
         for j, s in enumerate(stages):
             stage_ms[s] += e[j].elapsed_time(e[j + 1])
     stage_ms = {s: v / args.steps for s, v in stage_ms.items()}
+    pass_step_ms = sorted(e[0].elapsed_time(e[len(stages)]) for e in evs)
     ms_per_step = total_ms / args.steps
     value = pairs_per_second(R_total, args.steps, total_ms)
 
@@ -485,6 +486,14 @@ def main():
             d.update({"alg_flops": alg[s]["flops"], "TFLOP/s": round(tf, 1),
                       "frac_bf16_sustained": round(tf / pk["bf16_tflops_sustained"], 4)})
         stage_info[s] = d
+    # the memory-bound stages together (score, selection, compaction, scatter): their bytes over their
+    # summed time, against the same HBM bar as each of them
+    mem = [s for s in stages if s != "grouped"]
+    mem_ms = sum(stage_ms[s] for s in mem)
+    mem_bytes = sum(alg[s]["bytes"] for s in mem)
+    mem_gbs = mem_bytes / (mem_ms / 1e3) / 1e9
+    memory_stages = {"stages": mem, "ms": round(mem_ms, 4), "alg_bytes": mem_bytes, "GB/s": round(mem_gbs, 1),
+                     "frac_hbm": round(mem_gbs / pk["hbm_gbs"], 4)}
     dom = max(stages, key=lambda s: stage_ms[s])
     tr = recorded_traffic(dom, wl.name)
     # the binding roofline of the dominant stage is the one whose ideal time is longer
@@ -519,7 +528,10 @@ def main():
                          "through a 129 MB L2"},
         "roofline": roof,
         "stages": stage_info,
+        "memory_stages": memory_stages,
         "stages_pass": {"ms_per_step": round(sum(stage_ms.values()), 4),
+                        "step_ms_median": round(pass_step_ms[len(pass_step_ms) // 2], 4),
+                        "step_ms_min": round(pass_step_ms[0], 4),
                         "how": "a second pass of the same steps with an event at every stage boundary"},
         "e2e": e2e,
         "gpu_launches": launches * args.steps,
