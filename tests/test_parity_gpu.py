@@ -95,6 +95,12 @@ SMALL = [
     # T*k = 131072 pairs: selection leaves the rows in bucket order and scatters row_of_pair in a
     # launch of its own (the path of the large workloads), on shapes the oracle checks in full
     W.small_workload("bf16_deferred_rows", 16384, 64, 64, 64, 8),
+    # the limits of the ABI: top-1 routing, top-16 (LRM_MAX_TOPK: the generic score kernel, 16
+    # rows per token in compaction and scatter), and 1024 experts (LRM_MAX_EXPERTS: one plan and
+    # selection thread per expert, most experts holding a few rows)
+    W.small_workload("bf16_top1", 1000, 256, 128, 16, 1),
+    W.small_workload("bf16_top16", 600, 256, 128, 64, 16),
+    W.small_workload("bf16_e1024", 4096, 128, 64, 1024, 8),
 ]
 
 
